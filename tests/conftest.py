@@ -1,0 +1,23 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
+    config.addinivalue_line("markers", "slow: long-running test (large workloads)")
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _host_libs():
+    """Compile the generator and the oracle once per session."""
+    import oracle
+    import synth
+    synth.build()
+    oracle.build()
+    yield
