@@ -1,0 +1,417 @@
+// pi_abi.cu — host side of the libpi C ABI (declared in include/pi.h):
+// argument validation, workspace layout, launch configuration.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+#include <unordered_map>
+
+#include "kernels.cuh"
+
+using namespace pik;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Byte offsets of the workspace regions.
+struct WsLayout {
+  size_t ctrl, upart, loc_cnt, loc_idx, part, u, logits, total;
+};
+
+WsLayout ws_layout(const pi_ffn_desc& D, int batch) {
+  WsLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += round_up(bytes > 0 ? bytes : 1, kAlign);
+    return o;
+  };
+  L.ctrl = take(256);  // barrier counter (+0) and generation (+128)
+  L.upart = take(sizeof(float) * (size_t)D.r * kSMax);
+  L.loc_cnt = take(sizeof(int) * kPMax);
+  L.loc_idx = take(sizeof(int) * (size_t)D.n);
+  L.part = take(sizeof(float) * (size_t)kPMax * D.d);
+  L.u = take(sizeof(float) * (size_t)batch * D.r);
+  L.logits = take(sizeof(float) * (size_t)batch * D.n);
+  L.total = off;
+  return L;
+}
+
+pi_status check_desc(const pi_ffn_desc* D) {
+  if (!D) return PI_ERR_NULL;
+  if (D->dtype != PI_F16 && D->dtype != PI_BF16) return PI_ERR_DTYPE;
+  if (D->d < 8 || D->d > 8192 || (D->d & 7)) return PI_ERR_SHAPE;
+  if (D->r < 8 || D->r > 256 || (D->r & 7)) return PI_ERR_SHAPE;
+  if (D->n < 1 || D->n > (1 << 24)) return PI_ERR_SHAPE;
+  if (D->gated != 0 && D->gated != 1) return PI_ERR_SHAPE;
+  if (D->hot_prefix < 0 || D->hot_prefix > D->n) return PI_ERR_SHAPE;
+  return PI_OK;
+}
+
+pi_status check_weights(const pi_ffn_desc& D, const pi_layer_weights* w, bool need_pred) {
+  if (!w) return PI_ERR_NULL;
+  if (!w->b1 || !w->W1 || !w->W2) return PI_ERR_NULL;
+  if (need_pred && (!w->A || !w->Bm)) return PI_ERR_NULL;
+  const void* ps[] = {w->A, w->Bm, w->b1, w->W1, w->W2, w->b2};
+  for (const void* p : ps)
+    if (p && !aligned16(p)) return PI_ERR_ALIGN;
+  (void)D;
+  return PI_OK;
+}
+
+struct DevInfo {
+  int sms = 0;
+  int smem_optin = 0;
+};
+
+std::mutex g_mu;
+std::unordered_map<int, DevInfo> g_dev;
+std::unordered_map<const void*, int> g_smem_set;  // kernel -> dynamic smem attribute set (per process)
+unsigned long long g_limit_ns = 0;
+
+pi_status dev_info(DevInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PI_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_dev.find(dev);
+  if (it == g_dev.end()) {
+    DevInfo di;
+    if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&di.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess)
+      return PI_ERR_CUDA;
+    it = g_dev.emplace(dev, di).first;
+  }
+  *out = it->second;
+  return PI_OK;
+}
+
+unsigned long long wait_limit_ns() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_limit_ns == 0) {
+    g_limit_ns = 1000000000ull;  // 1 s
+    if (const char* e = std::getenv("PI_WAIT_LIMIT_NS")) {
+      const unsigned long long v = std::strtoull(e, nullptr, 10);
+      if (v >= 1000ull && v <= 10000000000ull) g_limit_ns = v;
+    }
+  }
+  return g_limit_ns;
+}
+
+pi_status ensure_smem(const void* fn, int bytes) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int& cur = g_smem_set[fn];  // per process; the attribute applies to the current device
+  if (bytes > cur) {
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+      return PI_ERR_CUDA;
+    cur = bytes;
+  }
+  return PI_OK;
+}
+
+pi_status map_launch_error(cudaError_t e) {
+  if (e == cudaSuccess) return PI_OK;
+  if (e == cudaErrorCooperativeLaunchTooLarge) return PI_ERR_LAUNCH;
+  return PI_ERR_CUDA;
+}
+
+using FfnFn = void (*)(const FfnArgs);
+
+template <int MODE>
+FfnFn pick_ffn(int dtype, int gated, bool wide) {
+  if (dtype == PI_F16) {
+    if (!gated) return wide ? ffn_kernel<0, false, 2, 4, MODE> : ffn_kernel<0, false, 1, 8, MODE>;
+    return wide ? ffn_kernel<0, true, 2, 2, MODE> : ffn_kernel<0, true, 1, 4, MODE>;
+  }
+  if (!gated) return wide ? ffn_kernel<1, false, 2, 4, MODE> : ffn_kernel<1, false, 1, 8, MODE>;
+  return wide ? ffn_kernel<1, true, 2, 2, MODE> : ffn_kernel<1, true, 1, 4, MODE>;
+}
+
+// Fills the shape fields, grid size and shared-memory layout of a
+// persistent launch; returns the dynamic shared-memory bytes (0 = error).
+int plan_ffn(const pi_ffn_desc& D, int mode, int P, int positions, FfnArgs& a) {
+  a.d = D.d;
+  a.n = D.n;
+  a.r = D.r;
+  a.P = P;
+  a.hot = D.hot_prefix;
+  a.nch = D.d / 8;
+  a.rows_max = (positions + P - 1) / P;
+  int S = 1;
+  while (D.r * S < P && S < kSMax && (D.d / (2 * S)) % 8 == 0 && D.d / (2 * S) >= 256) S *= 2;
+  a.S = S;
+  int off = 0;
+  auto take = [&](int bytes) {
+    const int o = off;
+    off += (bytes + 15) & ~15;
+    return o;
+  };
+  a.o_xs = take(4 * D.d);
+  a.o_wl = take(4 * a.rows_max);
+  a.o_red = take(16 * kThreads);
+  a.o_us = a.o_As = a.o_b1s = a.o_flag = a.o_lst = a.o_off = 0;
+  if (mode == kFused) {
+    a.o_us = take(4 * D.r);
+    a.o_As = take(2 * a.rows_max * D.r);
+    a.o_b1s = take(4 * a.rows_max);
+    a.o_flag = take(4 * a.rows_max);
+    a.o_lst = take(4 * a.rows_max);
+    a.o_off = take(4 * (P + 1));
+  }
+  return off;
+}
+
+template <int MODE>
+pi_status launch_ffn(const pi_ffn_desc& D, FfnArgs& a, int positions, cudaStream_t st) {
+  DevInfo di;
+  pi_status s = dev_info(&di);
+  if (s != PI_OK) return s;
+  const int P = di.sms < kPMax ? di.sms : kPMax;
+  const bool wide = (D.d / 8) > kThreads;
+  FfnFn fn = pick_ffn<MODE>(D.dtype, D.gated, wide);
+  const int smem = plan_ffn(D, MODE, P, positions, a);
+  if (smem + 1024 > di.smem_optin) return PI_ERR_SHAPE;
+  s = ensure_smem(reinterpret_cast<const void*>(fn), smem);
+  if (s != PI_OK) return s;
+  a.limit_ns = wait_limit_ns();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)P);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return map_launch_error(cudaLaunchKernelEx(&cfg, fn, a));
+}
+
+void bind_ws(FfnArgs& a, const WsLayout& L, void* ws) {
+  char* b = static_cast<char*>(ws);
+  a.bar.count = reinterpret_cast<unsigned*>(b + L.ctrl);
+  a.bar.gen = reinterpret_cast<unsigned*>(b + L.ctrl + 128);
+  a.upart = reinterpret_cast<float*>(b + L.upart);
+  a.loc_cnt = reinterpret_cast<int*>(b + L.loc_cnt);
+  a.loc_idx = reinterpret_cast<int*>(b + L.loc_idx);
+  a.part = reinterpret_cast<float*>(b + L.part);
+}
+
+void bind_weights(FfnArgs& a, const pi_layer_weights& w) {
+  a.A = static_cast<const uint16_t*>(w.A);
+  a.Bm = static_cast<const uint16_t*>(w.Bm);
+  a.b1 = w.b1;
+  a.W1 = static_cast<const uint16_t*>(w.W1);
+  a.W2 = static_cast<const uint16_t*>(w.W2);
+  a.b2 = w.b2;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pi_workspace_size(const pi_ffn_desc* desc, int32_t batch) {
+  if (check_desc(desc) != PI_OK) return 0;
+  if (batch < 1 || batch > kMaxBatch) return 0;
+  return ws_layout(*desc, batch).total;
+}
+
+const char* pi_status_string(pi_status s) {
+  switch (s) {
+    case PI_OK: return "ok";
+    case PI_ERR_NULL: return "a required pointer is NULL";
+    case PI_ERR_SHAPE: return "a size or the batch is outside the supported range";
+    case PI_ERR_DTYPE: return "dtype must be PI_F16 or PI_BF16";
+    case PI_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case PI_ERR_WORKSPACE: return "workspace smaller than pi_workspace_size()";
+    case PI_ERR_CAPACITY: return "more active neurons than the index list holds";
+    case PI_ERR_LAUNCH: return "the persistent grid cannot be co-resident on this GPU";
+    case PI_ERR_TIMEOUT: return "a bounded grid-wide wait ran out";
+    case PI_ERR_CUDA: return "a CUDA runtime call failed";
+    case PI_ERR_INDEX: return "an active-list entry is outside [0, n)";
+  }
+  return "unknown status";
+}
+
+pi_status pi_predict(const pi_ffn_desc* desc, const void* A, const void* Bm, const float* b1,
+                     const float* x, int32_t batch, float* logits, void* ws, size_t ws_bytes,
+                     pi_stream stream) {
+  pi_status s = check_desc(desc);
+  if (s != PI_OK) return s;
+  if (batch < 1 || batch > kMaxBatch) return PI_ERR_SHAPE;
+  if (!A || !Bm || !b1 || !x || !logits || !ws) return PI_ERR_NULL;
+  const void* ps[] = {A, Bm, b1, x, logits, ws};
+  for (const void* p : ps)
+    if (!aligned16(p)) return PI_ERR_ALIGN;
+  const WsLayout L = ws_layout(*desc, batch);
+  if (ws_bytes < L.total) return PI_ERR_WORKSPACE;
+  const pi_ffn_desc& D = *desc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  float* u = reinterpret_cast<float*>(static_cast<char*>(ws) + L.u);
+  const uint16_t* Bh = static_cast<const uint16_t*>(Bm);
+  const uint16_t* Ah = static_cast<const uint16_t*>(A);
+  const int tb = batch == 1 ? 1 : (batch <= 8 ? 8 : 32);
+  const bool bf = D.dtype == PI_BF16;
+#define PI_U(DT, TB) predict_u_kernel<DT, TB><<<D.r, 256, 0, st>>>(Bh, x, D.d, D.r, batch, u)
+  if (!bf) {
+    if (tb == 1) PI_U(0, 1); else if (tb == 8) PI_U(0, 8); else PI_U(0, 32);
+  } else {
+    if (tb == 1) PI_U(1, 1); else if (tb == 8) PI_U(1, 8); else PI_U(1, 32);
+  }
+#undef PI_U
+  if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
+  int rc = D.r / 8, G = 1;
+  while (G < rc) G <<= 1;
+  const int rows_per_block = 8 * (32 / G) * 4;
+  const unsigned grid = (unsigned)((D.n + rows_per_block - 1) / rows_per_block);
+  const size_t smem = sizeof(float) * (size_t)batch * D.r;
+#define PI_L(DT, TB) \
+  predict_logits_kernel<DT, TB><<<grid, 256, smem, st>>>(Ah, b1, u, D.n, D.r, batch, logits)
+  if (!bf) {
+    if (tb == 1) PI_L(0, 1); else if (tb == 8) PI_L(0, 8); else PI_L(0, 32);
+  } else {
+    if (tb == 1) PI_L(1, 1); else if (tb == 8) PI_L(1, 8); else PI_L(1, 32);
+  }
+#undef PI_L
+  if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
+  return PI_OK;
+}
+
+pi_status pi_compact(const float* logits, int32_t n, int32_t batch, int32_t* idx, int32_t* cnt,
+                     int32_t cap, int32_t* union_idx, int32_t* union_cnt, uint32_t* tok_mask,
+                     int32_t* dev_status, void* ws, size_t ws_bytes, pi_stream stream) {
+  (void)ws;
+  (void)ws_bytes;
+  if (n < 1 || n > (1 << 24) || batch < 1 || batch > kMaxBatch || cap < 0) return PI_ERR_SHAPE;
+  if (!logits || !idx || !cnt) return PI_ERR_NULL;
+  if (cap < n && !dev_status) return PI_ERR_NULL;
+  if (union_idx && (!union_cnt || !tok_mask)) return PI_ERR_NULL;
+  const void* ps[] = {logits, idx, cnt, union_idx, union_cnt, tok_mask, dev_status};
+  for (const void* p : ps)
+    if (p && !aligned16(p)) return PI_ERR_ALIGN;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  compact_kernel<<<batch, 1024, 0, st>>>(logits, n, idx, cnt, cap, dev_status);
+  if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
+  if (union_idx) {
+    union_kernel<<<1, 1024, 0, st>>>(logits, n, batch, union_idx, union_cnt, tok_mask);
+    if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
+  }
+  return PI_OK;
+}
+
+pi_status pi_sparse_ffn(const pi_ffn_desc* desc, const pi_layer_weights* w, const float* x,
+                        int32_t batch, const int32_t* idx, const int32_t* cnt, int32_t cap,
+                        const int32_t* union_idx, const int32_t* union_cnt,
+                        const uint32_t* tok_mask, float* y, int32_t* dev_status, void* ws,
+                        size_t ws_bytes, pi_stream stream) {
+  (void)union_idx;
+  (void)union_cnt;
+  (void)tok_mask;
+  pi_status s = check_desc(desc);
+  if (s != PI_OK) return s;
+  if (batch != 1) return PI_ERR_SHAPE;
+  s = check_weights(*desc, w, false);
+  if (s != PI_OK) return s;
+  if (!x || !y || !idx || !cnt || !dev_status || !ws) return PI_ERR_NULL;
+  const void* ps[] = {x, y, idx, cnt, dev_status, ws};
+  for (const void* p : ps)
+    if (!aligned16(p)) return PI_ERR_ALIGN;
+  if (cap < 0) return PI_ERR_SHAPE;
+  const WsLayout L = ws_layout(*desc, batch);
+  if (ws_bytes < L.total) return PI_ERR_WORKSPACE;
+  FfnArgs a{};
+  bind_weights(a, *w);
+  bind_ws(a, L, ws);
+  a.x = x;
+  a.residual = nullptr;
+  a.y = y;
+  a.idx_in = idx;
+  a.cnt_in = cnt;
+  a.cap = cap;
+  a.status = dev_status;
+  const int positions = cap < desc->n ? cap : desc->n;
+  return launch_ffn<kSparse>(*desc, a, positions > 0 ? positions : 1,
+                             reinterpret_cast<cudaStream_t>(stream));
+}
+
+pi_status pi_dense_ffn(const pi_ffn_desc* desc, const pi_layer_weights* w, const float* x,
+                       int32_t batch, float* y, void* ws, size_t ws_bytes, pi_stream stream) {
+  pi_status s = check_desc(desc);
+  if (s != PI_OK) return s;
+  if (batch < 1 || batch > kMaxBatch) return PI_ERR_SHAPE;
+  s = check_weights(*desc, w, false);
+  if (s != PI_OK) return s;
+  if (!x || !y || !ws) return PI_ERR_NULL;
+  const void* ps[] = {x, y, ws};
+  for (const void* p : ps)
+    if (!aligned16(p)) return PI_ERR_ALIGN;
+  const WsLayout L = ws_layout(*desc, batch);
+  if (ws_bytes < L.total) return PI_ERR_WORKSPACE;
+  for (int t = 0; t < batch; ++t) {
+    FfnArgs a{};
+    bind_weights(a, *w);
+    bind_ws(a, L, ws);
+    a.x = x + (size_t)t * desc->d;
+    a.residual = nullptr;
+    a.y = y + (size_t)t * desc->d;
+    a.status = nullptr;
+    s = launch_ffn<kDense>(*desc, a, desc->n, reinterpret_cast<cudaStream_t>(stream));
+    if (s != PI_OK) return s;
+  }
+  return PI_OK;
+}
+
+pi_status pi_layer_decode(const pi_ffn_desc* desc, const pi_layer_weights* w, const float* x,
+                          int32_t batch, float* y, const float* residual, int32_t* idx_out,
+                          int32_t* cnt_out, int32_t* dev_status, void* ws, size_t ws_bytes,
+                          pi_stream stream) {
+  pi_status s = check_desc(desc);
+  if (s != PI_OK) return s;
+  if (batch < 1 || batch > kMaxBatch) return PI_ERR_SHAPE;
+  s = check_weights(*desc, w, true);
+  if (s != PI_OK) return s;
+  if (!x || !y || !dev_status || !ws) return PI_ERR_NULL;
+  const void* ps[] = {x, y, residual, idx_out, cnt_out, dev_status, ws};
+  for (const void* p : ps)
+    if (p && !aligned16(p)) return PI_ERR_ALIGN;
+  const WsLayout L = ws_layout(*desc, batch);
+  if (ws_bytes < L.total) return PI_ERR_WORKSPACE;
+  const size_t d = (size_t)desc->d, n = (size_t)desc->n;
+  for (int t = 0; t < batch; ++t) {
+    FfnArgs a{};
+    bind_weights(a, *w);
+    bind_ws(a, L, ws);
+    a.x = x + t * d;
+    a.residual = residual ? residual + t * d : nullptr;
+    a.y = y + t * d;
+    a.idx_out = idx_out ? idx_out + t * n : nullptr;
+    a.cnt_out = cnt_out ? cnt_out + t : nullptr;
+    a.status = dev_status;
+    s = launch_ffn<kFused>(*desc, a, desc->n, reinterpret_cast<cudaStream_t>(stream));
+    if (s != PI_OK) return s;
+  }
+  return PI_OK;
+}
+
+pi_status pi_selftest_wait_timeout(int32_t* dev_status, void* ws, size_t ws_bytes,
+                                   int64_t limit_ns, pi_stream stream) {
+  if (!dev_status || !ws) return PI_ERR_NULL;
+  if (!aligned16(dev_status) || !aligned16(ws)) return PI_ERR_ALIGN;
+  if (ws_bytes < 256) return PI_ERR_WORKSPACE;
+  if (limit_ns < 1000 || limit_ns > 5000000000LL) return PI_ERR_SHAPE;
+  GridBar bar;
+  bar.count = static_cast<unsigned*>(ws);
+  bar.gen = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + 128);
+  wait_timeout_kernel<<<4, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      bar, dev_status, (unsigned long long)limit_ns);
+  if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
+  return PI_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,480 @@
+"""Decode benchmark of the activation-sparse FFN on GB300.
+
+One step = one batch-1 decode step of one FFN layer through pi_layer_decode
+(predictor, compaction, row-gather GEMV + ReLU, row-axpy down projection,
+deterministic split reduction: one persistent kernel launch).  The default
+workload is the OPT-6.7B-shaped FFN (d=4096, n=16384, r=128, fp16 weights,
+Zipf(0.9) activation profile at 6 % mean density), seeded and synthetic.
+
+Each step reads a different copy of the layer's weights (rotating
+replicas whose total is several times the L2 size), so every step's
+weights come from HBM; x is fresh per step.  Steps run as CUDA-graph
+replays; timing uses CUDA events on the launching stream.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank decodes its own token stream on its own
+GPU (replicas only: the path has no exchange step); rank 0 prints the
+aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sparse-FFN decode tokens/s at batch 1; achieved HBM GB/s vs peak (active bytes)"
+DEFAULT_WORKLOAD = "opt6.7b_ffn_d4096_n16384_r128_f16"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+# ------------------------------------------------------------------ helpers
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def aggregate(per_rank_ms, per_rank_units, n_gpus):
+    """Whole-job throughput: all ranks' units over the slowest rank's time."""
+    t = max(per_rank_ms)
+    return (sum(per_rank_units) / (t / 1e3)) if t > 0 else 0.0, t
+
+
+def csrc_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "activation_sparse_decode_rank_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(d, f), "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "pi.h"), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return float(j["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def stored_traffic(kernel_key):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    try:
+        j = json.load(open(PROFILE_TRAFFIC))
+    except Exception:
+        return None
+    e = j.get(kernel_key)
+    if not e or e.get("csrc_hash") != csrc_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ workload
+def workload_spec(name):
+    from synth.workloads import WORKLOADS
+    w = dict(WORKLOADS[name])
+    if w.get("layers", 1) != 1 or "densities" in w:
+        raise SystemExit(f"bench: workload {name} is not a single-layer batch-1 workload")
+    return w
+
+
+def hot_prefix_len(w):
+    import synth
+    c = synth.zipf_calibrate(w["n"], w["alpha"], w["density"])
+    p = synth.zipf_probs(w["n"], w["alpha"], c)
+    return int((p >= 0.5).sum())
+
+
+def cpu_oracle_sample(w, budget_s, max_tokens, warm=3):
+    """Times the fp64 oracle (predict + compact + sparse FFN) on the host
+    cores over a bounded sample of the workload's decode steps: at most
+    max_tokens steps, stopping once budget_s of oracle time is spent.  Input
+    generation is outside the timed part."""
+    import oracle
+    import synth
+    L = synth.make_layer(w["d"], w["n"], w["r"], w["dtype"], gated=w["gated"], alpha=w["alpha"],
+                         density=w["density"], seed=w["seed"])
+    for s in range(warm):
+        oracle.layer_decode(L, synth.gen_x(w["seed"], s, 1, w["d"])[0])
+    spent = 0.0
+    done = 0
+    for s in range(max_tokens):
+        x = synth.gen_x(w["seed"], s, 1, w["d"])[0]
+        t0 = time.perf_counter()
+        oracle.layer_decode(L, x)
+        spent += time.perf_counter() - t0
+        done += 1
+        if spent > budget_s:
+            break
+    return done, spent, oracle.get_threads()
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = workload_spec(args.workload)
+    budget = float(os.environ.get("PI_REF_BUDGET_S", "30"))
+    warm = min(args.warmup, 3)
+    done, dt, cores = cpu_oracle_sample(w, budget_s=budget, max_tokens=args.steps, warm=warm)
+    v = done / dt
+    sample = (f"{done} of {args.steps} requested decode steps of {args.workload} "
+              f"(time-bounded at {budget:.0f} s), fp64 oracle on {cores} host threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+        "n_gpus": world, "steps": done, "warmup": warm, "ms_per_step": dt / done * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "batch": 1, "density": w["density"]},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args):
+    import torch
+
+    import activation_sparse_decode_rank_gb300 as pi
+    import synth
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pi.build()
+    w = workload_spec(args.workload)
+    d, n, r = w["d"], w["n"], w["r"]
+    gated = bool(w["gated"])
+    m_rows = 3 if gated else 2
+    hot = hot_prefix_len(w) if args.hot < 0 else args.hot
+
+    L = synth.make_layer(d, n, r, w["dtype"], gated=gated, alpha=w["alpha"],
+                         density=w["density"], seed=w["seed"])
+
+    def up(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        return torch.from_numpy(a).to(dev)
+
+    # rotating weight replicas: every step reads a copy no other recent step touched
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2**20)
+    pred_bytes = n * r * 2 + r * d * 2 + n * 4
+    step_bytes_est = pred_bytes + w["density"] * n * m_rows * d * 2
+    R = args.replicas if args.replicas > 0 else max(2, math.ceil(3 * l2 / step_bytes_est))
+    base = [up(L.A), up(L.Bm), up(L.b1), up(L.W1), up(L.W2), up(L.b2)]
+    reps = [base] + [[t.clone() for t in base] for _ in range(R - 1)]
+    layer_bytes = sum(t.numel() * t.element_size() for t in base)
+    desc = pi.make_desc(d, n, r, w["dtype"], gated, hot)
+    wts = [pi.make_weights(*rp) for rp in reps]
+
+    G = min(args.steps, args.graph_len)
+    xs = torch.from_numpy(np.concatenate(
+        [synth.gen_x(w["seed"] + 1000 * rank, s, 1, d) for s in range(G)])).to(dev)
+    y = torch.empty((1, d), dtype=torch.float32, device=dev)
+    cnts = torch.zeros((G, 4), dtype=torch.int32, device=dev)  # 16-byte rows
+    st = torch.zeros(4, dtype=torch.int32, device=dev)
+    ws = pi.workspace(desc, 1, dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(s, cnt_slot=True, wt=None, xsrc=None, ydst=None):
+        rc = pi.pi_layer_decode(desc, wts[s % R] if wt is None else wt,
+                                xs[s % G] if xsrc is None else xsrc, 1,
+                                y if ydst is None else ydst, None, None,
+                                cnts[s % G] if cnt_slot else None, st, ws, stream=stream)
+        pi.check(rc, "pi_layer_decode")
+
+    def capture(nsteps, fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for s in range(nsteps):
+                    fn(s)
+        return g
+
+    with torch.cuda.stream(stream):
+        for s in range(min(G, 8)):   # eager run first: attribute setup, sanity
+            step(s)
+        stream.synchronize()
+        if int(st[0]) != 0:
+            raise SystemExit(f"bench: device status {pi.status_string(int(st[0]))}")
+    g_main = capture(G, step)
+    tail = args.steps % G
+    g_tail = capture(tail, step) if tail else None
+    g_warm = capture(min(args.warmup, G), step)
+
+    def replay_steps(k):
+        full, rem = divmod(k, G)
+        for _ in range(full):
+            g_main.replay()
+        if rem:
+            g_tail.replay()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # warmup (untimed): at least W steps
+    with torch.cuda.stream(stream):
+        gw = min(args.warmup, G)
+        for _ in range(math.ceil(args.warmup / gw)):
+            g_warm.replay()
+        stream.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        replay_steps(args.steps)
+        e1.record(stream)
+    stream.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1)
+    if int(st[0]) != 0:
+        raise SystemExit(f"bench: device status {pi.status_string(int(st[0]))}")
+
+    # byte accounting from the run's own active counts
+    cnt_host = cnts[:, 0].cpu().numpy().astype(np.float64)
+    mean_cnt = float(cnt_host.mean())
+    active_bytes = mean_cnt * m_rows * d * 2
+    alg_bytes = pred_bytes + active_bytes
+
+    # max over ranks
+    ms_all = [ms]
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_all = [float(tt.item())]
+    value, t_max = aggregate(ms_all, [args.steps * world], world)
+    ms_per_step = t_max / args.steps
+    per_launch_s = ms / args.steps / 1e3
+    peak, peak_kind = measured_peaks()
+    achieved = alg_bytes / per_launch_s / 1e9
+
+    # dense-FFN comparison point (same replicas, same protocol)
+    dense_steps = min(200, args.steps)
+    ws_d = pi.workspace(desc, 1, dev)
+
+    def dstep(s):
+        pi.check(pi.pi_dense_ffn(desc, wts[s % R], xs[s % G], 1, y, ws_d, stream=stream))
+
+    with torch.cuda.stream(stream):
+        for s in range(2):
+            dstep(s)
+    g_dense = capture(dense_steps, dstep)
+    with torch.cuda.stream(stream):
+        g_dense.replay()
+        d0 = torch.cuda.Event(enable_timing=True)
+        d1 = torch.cuda.Event(enable_timing=True)
+        d0.record(stream)
+        g_dense.replay()
+        d1.record(stream)
+    stream.synchronize()
+    dense_ms = d0.elapsed_time(d1) / dense_steps
+    dense_bytes = n * m_rows * d * 2 + n * 4
+
+    # end to end through the C ABI with host buffers: per step a pinned
+    # host -> device copy of x, the decode call, a device -> host copy of y
+    e2e_steps = min(args.steps, args.e2e_steps)
+    xh = torch.from_numpy(np.concatenate(
+        [synth.gen_x(w["seed"] + 7 + 1000 * rank, s, 1, d) for s in range(G)])).pin_memory()
+    yh = torch.empty((G, d), dtype=torch.float32).pin_memory()
+    xin = torch.empty((1, d), dtype=torch.float32, device=dev)
+
+    def estep(s):
+        xin.copy_(xh[s % G:s % G + 1], non_blocking=True)
+        step(s, cnt_slot=False, xsrc=xin)
+        yh[s % G:s % G + 1].copy_(y, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for s in range(2):
+            estep(s)
+    stream.synchronize()
+    g_e2e = capture(G, estep)
+    with torch.cuda.stream(stream):
+        g_e2e.replay()
+        stream.synchronize()
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        full = max(1, e2e_steps // G)
+        for _ in range(full):
+            g_e2e.replay()
+        f1.record(stream)
+    stream.synchronize()
+    e2e_ms = f0.elapsed_time(f1)
+    e2e_done = full * G
+    e2e_ms_all = [e2e_ms]
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms_all = [float(tt.item())]
+    e2e_value, _ = aggregate(e2e_ms_all, [e2e_done * world], world)
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        budget = float(os.environ.get("PI_CPU_BUDGET_S", "15"))
+        done, dt, cores = cpu_oracle_sample(w, budget_s=budget, max_tokens=100000)
+        cpu = {"value": done / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"first {done} decode steps of {args.workload} (time-bounded at "
+                         f"{budget:.0f} s), fp64 oracle predict+compact+sparse FFN"}
+
+    kernel_key = f"ffn_kernel_fused:{args.workload}"
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": args.workload, "batch": 1, "weights": w["dtype"], "density": w["density"],
+            "d": d, "n": n, "r": r, "gated": gated, "hot_prefix": hot,
+            "l2": (f"inputs larger than L2: {R} rotating weight replicas "
+                   f"({R * layer_bytes / 1e9:.1f} GB; each step reads its own copy)"),
+            "graph_len": G, "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "us_per_layer": ms_per_step * 1e3,
+        "active_neurons_mean": mean_cnt,
+        "bytes_per_step": {"predictor": pred_bytes, "active_rows": active_bytes,
+                           "total": alg_bytes},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": stored_traffic(kernel_key),
+                     "peak_kind": f"{peak_kind} copy bandwidth",
+                     "kernel": "ffn_kernel (fused predictor+compaction+FFN, one launch/step)"},
+        "dense_ffn": {"us_per_step": dense_ms * 1e3, "tokens_per_s": 1e3 / dense_ms,
+                      "achieved_gbs": dense_bytes / (dense_ms / 1e3) / 1e9,
+                      "frac": dense_bytes / (dense_ms / 1e3) / 1e9 / peak},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": d * 4,
+                "d2h_bytes_per_step": d * 4, "steps": e2e_done,
+                "how": "CUDA-graph replay of (pinned H2D x, pi_layer_decode, D2H y) per step"},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "csrc_hash": csrc_hash(),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200000)
+    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--replicas", type=int, default=0)
+    ap.add_argument("--hot", type=int, default=-1, help="hot-prefix length (-1: p_i >= 0.5)")
+    ap.add_argument("--graph-len", type=int, default=2000)
+    ap.add_argument("--e2e-steps", type=int, default=20000)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("bench: at least 3 warm-up steps")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

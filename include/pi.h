@@ -1,0 +1,198 @@
+/*
+ * pi.h — C ABI of the activation-sparse decode FFN library (libpi.so).
+ *
+ * The library implements the online part of the method described on the
+ * page "PowerInfer: Quick Massive Language Mannequin Serving with a
+ * Client-grade GPU": a predictor scores every FFN neuron, the neurons
+ * predicted inactive are skipped ("Online Section"), and neuron-aware
+ * operators compute only the rows of the up projection and the column
+ * vectors of the down projection that belong to activated neurons, directly
+ * on the stored matrices ("Neuron Conscious Operator").  Neurons are stored
+ * hot-first (most frequently active first, "Offline Section"), so the
+ * hot block is a contiguous prefix; neuron indices are positions in the
+ * stored matrices ("Neuron Placement and Administration").  Everything runs
+ * on one GPU; there is no CPU executor and no CPU fallback.
+ *
+ * Conventions for every call
+ * --------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *    library never allocates, frees or copies to the host on these calls.
+ *  - Calls are asynchronous on the caller's stream (NULL = legacy default
+ *    stream); they never synchronise the host.  Counts stay on the device,
+ *    so a sequence of calls can be captured in a CUDA graph.
+ *  - Layouts are row-major with one row per neuron:
+ *      A   [n][r]      predictor factor   (dtype)
+ *      Bm  [r][d]      predictor factor   (dtype)
+ *      b1  [n]         fp32 bias of the predictor and of the up projection
+ *                      (gated: of the gate)
+ *      W1  [n][d]      up projection, or gated [n][2][d]: per neuron the
+ *                      gate row followed by the up row        (dtype)
+ *      W2  [n][d]      down projection, one row per neuron   (dtype)
+ *      b2  [d]         fp32 output bias, may be NULL (= 0)
+ *      x   [batch][d]  fp32 activations;  y [batch][d] fp32 outputs
+ *  - Alignment: every pointer passed must be 16-byte aligned.
+ *  - Sizes: d % 8 == 0 and 8 <= d <= 8192; r % 8 == 0 and 8 <= r <= 256;
+ *    1 <= n <= 1 << 24; 1 <= batch <= 32 (sparse / fused paths: see each
+ *    call).
+ *  - Workspace: `ws` is caller-owned device scratch of at least
+ *    pi_workspace_size(desc, batch) bytes.  It must be zero-filled before
+ *    its first use; afterwards the library leaves it ready for the next
+ *    call.  One workspace serves one stream at a time (calls that overlap
+ *    on the GPU must use different workspaces).  After PI_ERR_TIMEOUT it
+ *    must be zero-filled again.
+ *  - Errors come on two channels.  Host-detected errors (NULL pointer, bad
+ *    size or dtype, misalignment, small workspace, grid that cannot be
+ *    co-resident, failed launch) are returned before or at launch; nothing
+ *    has been launched when the status is not PI_OK, except for PI_ERR_CUDA
+ *    raised by the launch itself.  Device-detected errors (capacity
+ *    exceeded, an index out of range, a bounded wait that ran out) are
+ *    written to *dev_status
+ *    (an int32 in device memory the caller zeroes; the first error wins)
+ *    and can be read after the caller synchronises its stream.
+ */
+#ifndef PI_H
+#define PI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st* pi_stream;
+
+typedef enum {
+  PI_OK = 0,
+  PI_ERR_NULL = 1,       /* a required pointer is NULL                         */
+  PI_ERR_SHAPE = 2,      /* a size or the batch is outside the supported range */
+  PI_ERR_DTYPE = 3,      /* dtype is not PI_F16 / PI_BF16                      */
+  PI_ERR_ALIGN = 4,      /* a pointer is not 16-byte aligned                   */
+  PI_ERR_WORKSPACE = 5,  /* ws_bytes < pi_workspace_size(desc, batch)          */
+  PI_ERR_CAPACITY = 6,   /* device: more active neurons than the list holds    */
+  PI_ERR_LAUNCH = 7,     /* the persistent grid cannot be co-resident          */
+  PI_ERR_TIMEOUT = 8,    /* device: a bounded grid-wide wait ran out           */
+  PI_ERR_CUDA = 9,       /* a CUDA runtime call failed                         */
+  PI_ERR_INDEX = 10      /* device: an active-list entry is outside [0, n)     */
+} pi_status;
+
+typedef enum { PI_F16 = 0, PI_BF16 = 1 } pi_dtype;
+
+/* Shape of one FFN layer. */
+typedef struct {
+  int32_t d;           /* model (hidden) dimension                              */
+  int32_t n;           /* FFN neurons                                           */
+  int32_t r;           /* predictor rank                                        */
+  int32_t dtype;       /* pi_dtype of A, Bm, W1, W2                             */
+  int32_t gated;       /* 0: h = ReLU(W1 x + b1); 1: h = ReLU(Wg x + b1)(Wu x)  */
+  int32_t hot_prefix;  /* neurons [0, hot_prefix) form the hot block: their
+                          rows are fetched towards the chip before the mask is
+                          known (0 = off).  Never changes results.             */
+} pi_ffn_desc;
+
+/* Device pointers of one layer's weights (layouts above). */
+typedef struct {
+  const void* A;
+  const void* Bm;
+  const float* b1;
+  const void* W1;
+  const void* W2;
+  const float* b2; /* may be NULL */
+} pi_layer_weights;
+
+/* Bytes of workspace the calls below need for this shape and batch.
+ * Returns 0 for an invalid descriptor or batch.  Host-only; no CUDA call. */
+size_t pi_workspace_size(const pi_ffn_desc* desc, int32_t batch);
+
+/* Predictor ("Adaptive Sparsity Predictors": the engine predicts which
+ * neurons will activate before computing the FFN; the predictor lives in
+ * GPU memory).  For each token t < batch:
+ *     u      = Bm x[t]                    (fp32 accumulate, kept fp32)
+ *     logits[t][i] = A_i . u + b1_i       (fp32)
+ * logits is [batch][n] fp32.  batch <= 32. */
+pi_status pi_predict(const pi_ffn_desc* desc, const void* A, const void* Bm,
+                     const float* b1, const float* x, int32_t batch,
+                     float* logits, void* ws, size_t ws_bytes,
+                     pi_stream stream);
+
+/* Compaction of the predicted mask into the active-neuron list ("Online
+ * Section": non-activated neurons are skipped; the list plays the part of
+ * the GPU-side neuron table).  For each token t:
+ *     idx[t][0 .. cnt[t]) = ascending { i : logits[t][i] > 0 }   (strict)
+ * idx is [batch][cap] int32, cnt is [batch] int32.  If cnt[t] > cap only the
+ * first cap entries are written, cnt[t] still holds the full count, and
+ * PI_ERR_CAPACITY is written to *dev_status.
+ * If union_idx is not NULL (batched decode) also:
+ *     union_idx[0 .. *union_cnt) = ascending { i : some token active }
+ *     tok_mask[k] bit t set iff token t is active at neuron union_idx[k]
+ * (capacity n for both; batch <= 32).  dev_status may be NULL only when no
+ * capacity error can occur (cap >= n). */
+pi_status pi_compact(const float* logits, int32_t n, int32_t batch,
+                     int32_t* idx, int32_t* cnt, int32_t cap,
+                     int32_t* union_idx, int32_t* union_cnt,
+                     uint32_t* tok_mask, int32_t* dev_status, void* ws,
+                     size_t ws_bytes, pi_stream stream);
+
+/* Neuron-aware sparse FFN ("Neuron Conscious Operator": only the activated
+ * neurons' row vectors of W1 and column vectors of W2 are touched, with no
+ * conversion to a dense or sparse format).  batch == 1:
+ *     h_k = ReLU(W1[idx[k]] . x + b1[idx[k]])
+ *           (gated: ReLU(Wg[idx[k]] . x + b1[idx[k]]) * (Wu[idx[k]] . x))
+ *     y   = b2 + sum_{k < cnt[0]} h_k W2[idx[k]]
+ * with fp32 accumulation and a fixed-order (deterministic) split reduction.
+ * idx / cnt are device arrays (e.g. from pi_compact); cnt[0] must be <= cap
+ * (else PI_ERR_CAPACITY on *dev_status and nothing is computed).  An entry
+ * outside [0, n) is not read: it contributes nothing and PI_ERR_INDEX is
+ * written to *dev_status.
+ * batch > 1: the union form; union_idx / union_cnt / tok_mask as written by
+ * pi_compact, and token t uses exactly the union neurons whose mask bit t is
+ * set, so y[t] equals the batch-1 result for token t. */
+pi_status pi_sparse_ffn(const pi_ffn_desc* desc, const pi_layer_weights* w,
+                        const float* x, int32_t batch, const int32_t* idx,
+                        const int32_t* cnt, int32_t cap,
+                        const int32_t* union_idx, const int32_t* union_cnt,
+                        const uint32_t* tok_mask, float* y,
+                        int32_t* dev_status, void* ws, size_t ws_bytes,
+                        pi_stream stream);
+
+/* Dense FFN over all n neurons, the comparison point of the sparse path:
+ *     y[t] = b2 + sum_i ReLU(W1_i . x[t] + b1_i) W2_i   (gated as above).
+ * batch <= 32. */
+pi_status pi_dense_ffn(const pi_ffn_desc* desc, const pi_layer_weights* w,
+                       const float* x, int32_t batch, float* y, void* ws,
+                       size_t ws_bytes, pi_stream stream);
+
+/* One decode step of one layer: predictor, compaction and sparse FFN
+ * ("Online Section" end to end).  batch == 1 runs as one persistent launch
+ * whose grid-wide waits are bounded (PI_ERR_TIMEOUT on *dev_status if one
+ * runs out).  batch > 1 runs the batched predictor, the union compaction
+ * and the batched sparse FFN.
+ *     y[t] = (residual ? residual[t] : 0) + FFN_sparse(x[t])
+ * residual may be NULL; pass residual = x for a residual stack.  idx_out
+ * ([batch][n]) and cnt_out ([batch]) may be NULL; when given they receive
+ * each token's ascending active list and count.  dev_status must not be
+ * NULL. */
+pi_status pi_layer_decode(const pi_ffn_desc* desc, const pi_layer_weights* w,
+                          const float* x, int32_t batch, float* y,
+                          const float* residual, int32_t* idx_out,
+                          int32_t* cnt_out, int32_t* dev_status, void* ws,
+                          size_t ws_bytes, pi_stream stream);
+
+/* Static text of a status code. */
+const char* pi_status_string(pi_status s);
+
+/* Diagnostic of the failure path: runs the persistent grid's bounded wait
+ * with one arrival that never comes, for limit_ns nanoseconds, so every
+ * block gives up and PI_ERR_TIMEOUT lands in *dev_status.  ws must be a
+ * zero-filled workspace of pi_workspace_size(desc, 1) bytes for some valid
+ * desc; it must be zero-filled again afterwards.  Returns PI_OK when the
+ * launch was issued. */
+pi_status pi_selftest_wait_timeout(int32_t* dev_status, void* ws,
+                                   size_t ws_bytes, int64_t limit_ns,
+                                   pi_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

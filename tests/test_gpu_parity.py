@@ -1,0 +1,337 @@
+"""GPU parity of every C-ABI entry point against the fp64 oracle.
+
+Workloads: the tiny ReLU layer and the OPT-6.7B-, Llama-2-7B- (gated) and
+OPT-30B-shaped layers at full size, a ragged layer whose sizes are not
+multiples of the tiles, and batched predictor cases of the OPT-13B shape.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import activation_sparse_decode_rank_gb300 as pi
+import oracle
+import synth
+from pihelp import DevLayer, Y_TOL, check_active_set, near_ties, up, y_rel_err, zeros_i32
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+# (name, d, n, r, dtype, gated, alpha, density, seed, hot_prefix)
+WL = {
+    "tiny_d1024_n4096": (1024, 4096, 64, "f16", False, 0.8, 0.08, 1, 90),
+    "ragged_d200_n1001_r24": (200, 1001, 24, "bf16", False, 0.9, 0.10, 11, 37),
+    "ragged_gated_d136_n777_r16": (136, 777, 16, "f16", True, 1.0, 0.12, 12, 0),
+    "opt6.7b_d4096_n16384": (4096, 16384, 128, "f16", False, 0.9, 0.06, 2, 304),
+    "llama2_7b_gated_d4096_n11008": (4096, 11008, 256, "bf16", True, 1.0, 0.10, 3, 463),
+    "opt30b_layer_d7168_n28672": (7168, 28672, 256, "f16", False, 0.9, 0.09, 4, 800),
+}
+_host = {}
+_dev = {}
+
+
+def layer(name):
+    """The named layer on the GPU (host copies are kept; one device copy)."""
+    if name not in _dev:
+        d, n, r, dt, g, a, rho, seed, hot = WL[name]
+        if name not in _host:
+            _host[name] = synth.make_layer(d, n, r, dt, gated=g, alpha=a, density=rho, seed=seed)
+        _dev.clear()
+        torch.cuda.empty_cache()
+        _dev[name] = DevLayer(_host[name], DEV, hot_prefix=hot)
+    return _dev[name]
+
+
+def logits_bound(L, x, u_ref):
+    """fp32 error bound of the GPU logits: stage-1 dot products of length d,
+    stage-2 of length r (+ bias), gamma_K = K u / (1 - K u), u = 2^-24."""
+    uu = 2.0**-24
+    g = lambda k: k * uu / (1 - k * uu)
+    dec = (lambda b: b.view(np.float16).astype(np.float64)) if L.dtype == "f16" else \
+        (lambda b: (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64))
+    A = np.abs(dec(L.A))
+    B = np.abs(dec(L.Bm))
+    du = g(L.d) * (B @ np.abs(x.astype(np.float64)))
+    return 2.0 * (A @ du + g(L.r + 1) * (A @ np.abs(u_ref) + np.abs(L.b1))) + 1e-30
+
+
+# ---------------------------------------------------------------- predictor
+@pytest.mark.parametrize("name", ["tiny_d1024_n4096", "ragged_d200_n1001_r24",
+                                  "opt6.7b_d4096_n16384", "llama2_7b_gated_d4096_n11008"])
+@pytest.mark.parametrize("batch", [1, 5])
+def test_predict_parity(name, batch):
+    D = layer(name)
+    L = D.L
+    x = synth.gen_x(100 + batch, 0, batch, L.d)
+    lg = torch.empty((batch, L.n), dtype=torch.float32, device=DEV)
+    ws = D.workspace(batch)
+    pi.check(pi.pi_predict(D.desc, D.A, D.Bm, D.b1, up(x, DEV), batch, lg, ws), "pi_predict")
+    torch.cuda.synchronize()
+    g = lg.cpu().numpy().astype(np.float64)
+    u, lo = oracle.predict(L, x)
+    for t in range(batch):
+        bound = logits_bound(L, x[t], u[t])
+        assert np.all(np.abs(g[t] - lo[t]) <= bound)
+        tie = near_ties(lo[t])
+        np.testing.assert_array_equal((g[t] > 0)[~tie], (lo[t] > 0)[~tie])
+
+
+def test_predict_batch32_opt13b_shape():
+    L = synth.make_layer(5120, 20480, 192, "f16", alpha=0.9, density=0.05, seed=5)
+    D = DevLayer(L, DEV)
+    x = synth.gen_x(5, 0, 32, 5120)
+    lg = torch.empty((32, L.n), dtype=torch.float32, device=DEV)
+    pi.check(pi.pi_predict(D.desc, D.A, D.Bm, D.b1, up(x, DEV), 32, lg, D.workspace(32)))
+    torch.cuda.synchronize()
+    g = lg.cpu().numpy().astype(np.float64)
+    u, lo = oracle.predict(L, x)
+    for t in (0, 13, 31):
+        assert np.all(np.abs(g[t] - lo[t]) <= logits_bound(L, x[t], u[t]))
+
+
+# ---------------------------------------------------------------- compaction
+def _compact(lg_host, cap, union=False, dev_status=True):
+    batch, n = lg_host.shape
+    lg = up(lg_host.astype(np.float32), DEV)
+    idx = torch.full((batch, max(cap, 1)), -7, dtype=torch.int32, device=DEV)
+    cnt = zeros_i32(batch, DEV)
+    st = zeros_i32(1, DEV)
+    ui = torch.full((n,), -7, dtype=torch.int32, device=DEV) if union else None
+    uc = zeros_i32(1, DEV) if union else None
+    tm = torch.zeros(n, dtype=torch.int32, device=DEV) if union else None
+    pi.check(pi.pi_compact(lg, n, batch, idx, cnt, cap, ui, uc, tm, st if dev_status else None,
+                           None, 0))
+    torch.cuda.synchronize()
+    out = dict(idx=idx.cpu().numpy(), cnt=cnt.cpu().numpy()[:batch], status=int(st[0]))
+    if union:
+        c = int(uc[0])
+        out.update(uidx=ui.cpu().numpy()[:c], tmask=tm.cpu().numpy().view(np.uint32)[:c])
+    return out
+
+
+@pytest.mark.parametrize("n", [1, 31, 1023, 1024, 1025, 4096, 28672, 100003])
+def test_compact_bit_exact(n):
+    rng = np.random.default_rng(n)
+    for density in (0.0, 0.07, 0.5, 1.0):
+        lg = np.where(rng.random((3, n)) < density, rng.random((3, n)) + 1e-3,
+                      -rng.random((3, n))).astype(np.float32)
+        lg[:, : min(n, 3)] = [0.0, -0.0, 1e-38][: min(n, 3)]  # zeros are inactive
+        o = _compact(lg, n)
+        assert o["status"] == 0
+        for t in range(3):
+            want = oracle.compact(lg[t].astype(np.float64))
+            assert o["cnt"][t] == len(want)
+            np.testing.assert_array_equal(o["idx"][t][: len(want)], want)
+
+
+def test_compact_capacity_overflow_reported():
+    lg = np.ones((2, 5000), np.float32)
+    lg[1, ::2] = -1.0
+    o = _compact(lg, 1000)
+    assert o["status"] == pi.PI_ERR_CAPACITY
+    assert list(o["cnt"]) == [5000, 2500]
+    np.testing.assert_array_equal(o["idx"][0], np.arange(1000))
+    np.testing.assert_array_equal(o["idx"][1], np.arange(1, 2001, 2))
+
+
+@pytest.mark.parametrize("batch", [1, 4, 16, 32])
+def test_union_bit_exact(batch):
+    rng = np.random.default_rng(batch)
+    lg = (rng.standard_normal((batch, 20480)) - 1.8).astype(np.float32)
+    o = _compact(lg, 20480, union=True)
+    want_i, want_m = oracle.union(lg.astype(np.float64))
+    np.testing.assert_array_equal(o["uidx"], want_i)
+    np.testing.assert_array_equal(o["tmask"], want_m)
+
+
+# ---------------------------------------------------------------- sparse / dense FFN
+def _sparse(D, x, idx_list, cap=None):
+    L = D.L
+    cap = L.n if cap is None else cap
+    idx = torch.zeros(max(cap, 1), dtype=torch.int32, device=DEV)
+    k = min(len(idx_list), cap)
+    if k:
+        idx[:k] = torch.from_numpy(np.asarray(idx_list[:k], np.int32)).to(DEV)
+    cnt = torch.tensor([len(idx_list), 0, 0, 0], dtype=torch.int32, device=DEV)
+    y = torch.full((1, L.d), float("nan"), device=DEV)
+    st = zeros_i32(1, DEV)
+    pi.check(pi.pi_sparse_ffn(D.desc, D.w, up(x, DEV), 1, idx, cnt, cap, None, None, None, y, st,
+                              D.workspace()))
+    torch.cuda.synchronize()
+    return y[0].cpu().numpy(), int(st[0])
+
+
+@pytest.mark.parametrize("name", list(WL))
+def test_sparse_ffn_parity(name):
+    D = layer(name)
+    L = D.L
+    x = synth.gen_x(7, 0, 1, L.d)
+    _, lo = oracle.predict(L, x)
+    idx = oracle.compact(lo[0])
+    y, st = _sparse(D, x, idx)
+    assert st == 0
+    assert y_rel_err(L, x, idx, y) <= Y_TOL
+
+
+def test_sparse_ffn_edge_lists():
+    D = layer("ragged_d200_n1001_r24")
+    L = D.L
+    x = synth.gen_x(8, 0, 1, L.d)
+    # empty list: y = b2
+    y, st = _sparse(D, x, [])
+    assert st == 0
+    np.testing.assert_array_equal(y, L.b2)
+    # every neuron (dense through the sparse operator)
+    y, st = _sparse(D, x, np.arange(L.n))
+    assert st == 0 and y_rel_err(L, x, np.arange(L.n), y) <= Y_TOL
+    # one neuron, the last one
+    y, st = _sparse(D, x, [L.n - 1])
+    assert st == 0 and y_rel_err(L, x, [L.n - 1], y) <= Y_TOL
+    # more active than the list holds: reported, nothing computed
+    y, st = _sparse(D, x, np.arange(50), cap=20)
+    assert st == pi.PI_ERR_CAPACITY
+    # an entry outside [0, n) is reported and skipped, never read
+    y, st = _sparse(D, x, [3, L.n, 7])
+    assert st == pi.PI_ERR_INDEX
+    y2, _ = _sparse(D, x, [3, 7])
+    np.testing.assert_array_equal(y, y2)
+
+
+@pytest.mark.parametrize("name", ["tiny_d1024_n4096", "ragged_gated_d136_n777_r16",
+                                  "opt6.7b_d4096_n16384", "llama2_7b_gated_d4096_n11008"])
+def test_dense_ffn_parity(name):
+    D = layer(name)
+    L = D.L
+    batch = 2
+    x = synth.gen_x(9, 0, batch, L.d)
+    y = torch.empty((batch, L.d), device=DEV)
+    pi.check(pi.pi_dense_ffn(D.desc, D.w, up(x, DEV), batch, y, D.workspace(batch)))
+    torch.cuda.synchronize()
+    for t in range(batch):
+        yd = oracle.dense_ffn(L, x[t])
+        err = float(np.abs(y[t].cpu().numpy() - yd).max()) / float(np.abs(yd).max())
+        assert err <= Y_TOL
+
+
+# ---------------------------------------------------------------- fused decode
+def _decode(D, x, batch=1, residual=None, want_idx=True):
+    L = D.L
+    xd = up(x, DEV)
+    y = torch.full((batch, L.d), float("nan"), device=DEV)
+    idx = torch.full((batch, L.n), -1, dtype=torch.int32, device=DEV) if want_idx else None
+    cnt = zeros_i32(batch, DEV) if want_idx else None
+    st = zeros_i32(1, DEV)
+    res = xd if residual else None
+    pi.check(pi.pi_layer_decode(D.desc, D.w, xd, batch, y, res, idx, cnt, st,
+                                D.workspace(batch)), "pi_layer_decode")
+    torch.cuda.synchronize()
+    out = dict(y=y.cpu().numpy(), status=int(st[0]))
+    if want_idx:
+        out["cnt"] = cnt.cpu().numpy()[:batch]
+        out["idx"] = [idx[t, : out["cnt"][t]].cpu().numpy() for t in range(batch)]
+    return out
+
+
+@pytest.mark.parametrize("name", list(WL))
+def test_layer_decode_parity(name):
+    D = layer(name)
+    L = D.L
+    steps = 3 if L.d >= 4096 else 6
+    ties = 0
+    for s in range(steps):
+        x = synth.gen_x(20 + s, s, 1, L.d)
+        o = _decode(D, x)
+        assert o["status"] == 0
+        _, lo = oracle.predict(L, x)
+        ties += check_active_set(o["idx"][0], lo[0])
+        assert y_rel_err(L, x, o["idx"][0], o["y"][0]) <= Y_TOL
+        if not np.any(near_ties(lo[0])):
+            # no near-ties: the end-to-end result must match too
+            np.testing.assert_array_equal(o["idx"][0], oracle.compact(lo[0]))
+    assert ties <= steps * 2
+
+
+def test_layer_decode_residual_and_hot_prefix_variants():
+    D = layer("ragged_d200_n1001_r24")
+    L = D.L
+    x = synth.gen_x(30, 0, 1, L.d)
+    base = _decode(D, x)
+    for hot in (0, 1, 500, L.n):
+        D.desc.hot_prefix = hot
+        o = _decode(D, x, residual=True)
+        # the hot prefix only changes what is fetched early, never the result
+        np.testing.assert_array_equal(o["idx"][0], base["idx"][0])
+        np.testing.assert_allclose(o["y"][0], base["y"][0] + x[0], rtol=0, atol=1e-6)
+    D.desc.hot_prefix = WL["ragged_d200_n1001_r24"][-1]
+    # without the optional outputs
+    o = _decode(D, x, want_idx=False)
+    np.testing.assert_array_equal(o["y"][0], base["y"][0])
+
+
+def test_layer_decode_deterministic():
+    D = layer("opt6.7b_d4096_n16384")
+    x = synth.gen_x(31, 0, 1, D.L.d)
+    a = _decode(D, x)
+    b = _decode(D, x)
+    np.testing.assert_array_equal(a["y"], b["y"])
+    np.testing.assert_array_equal(a["idx"][0], b["idx"][0])
+
+
+def test_layer_decode_batch_equals_per_token():
+    D = layer("tiny_d1024_n4096")
+    x = synth.gen_x(32, 0, 4, D.L.d)
+    ob = _decode(D, x, batch=4)
+    for t in range(4):
+        o1 = _decode(D, x[t:t + 1])
+        np.testing.assert_array_equal(ob["y"][t], o1["y"][0])
+        np.testing.assert_array_equal(ob["idx"][t], o1["idx"][0])
+
+
+def test_layer_decode_no_active_neuron():
+    L = synth.make_layer(256, 512, 16, "f16", alpha=0.9, density=0.1, seed=33)
+    L.b1[:] = -1e4  # every logit is negative
+    D = DevLayer(L, DEV)
+    x = synth.gen_x(33, 0, 1, 256)
+    o = _decode(D, x)
+    assert o["status"] == 0 and o["cnt"][0] == 0
+    np.testing.assert_array_equal(o["y"][0], L.b2)
+
+
+def test_layer_decode_in_cuda_graph():
+    D = layer("tiny_d1024_n4096")
+    L = D.L
+    x = up(synth.gen_x(34, 0, 1, L.d), DEV)
+    y = torch.empty((1, L.d), device=DEV)
+    st = zeros_i32(1, DEV)
+    ws = D.workspace()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        pi.check(pi.pi_layer_decode(D.desc, D.w, x, 1, y, None, None, None, st, ws, stream=s))
+        s.synchronize()
+        ref = y.clone()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            pi.check(pi.pi_layer_decode(D.desc, D.w, x, 1, y, None, None, None, st, ws,
+                                        stream=s))
+        y.zero_()
+        for _ in range(3):
+            g.replay()
+        s.synchronize()
+    assert int(st[0]) == 0
+    torch.testing.assert_close(y, ref, rtol=0, atol=0)
+
+
+# ---------------------------------------------------------------- failure path
+def test_bounded_wait_times_out_and_reports():
+    D = layer("tiny_d1024_n4096")
+    ws = D.workspace()
+    st = zeros_i32(1, DEV)
+    pi.check(pi.pi_selftest_wait_timeout(st, ws, 2_000_000))  # 2 ms
+    torch.cuda.synchronize()
+    assert int(st[0]) == pi.PI_ERR_TIMEOUT
+    # the context is still usable: a fresh workspace decodes normally
+    x = synth.gen_x(35, 0, 1, D.L.d)
+    o = _decode(D, x)
+    assert o["status"] == 0
