@@ -25,6 +25,7 @@ _lib = None
 PI_OK, PI_ERR_NULL, PI_ERR_SHAPE, PI_ERR_DTYPE, PI_ERR_ALIGN, PI_ERR_WORKSPACE, \
     PI_ERR_CAPACITY, PI_ERR_LAUNCH, PI_ERR_TIMEOUT, PI_ERR_CUDA, PI_ERR_INDEX = range(11)
 PI_F16, PI_BF16 = 0, 1
+PI_LAYOUT_SPLIT, PI_LAYOUT_PACKED = 0, 1
 
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC", "-shared"]
@@ -59,7 +60,7 @@ class PiError(RuntimeError):
 class pi_ffn_desc(ctypes.Structure):
     _fields_ = [("d", ctypes.c_int32), ("n", ctypes.c_int32), ("r", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("gated", ctypes.c_int32),
-                ("hot_prefix", ctypes.c_int32)]
+                ("hot_prefix", ctypes.c_int32), ("layout", ctypes.c_int32)]
 
 
 class pi_layer_weights(ctypes.Structure):
@@ -81,6 +82,7 @@ SIGNATURES = {
     "pi_layer_decode": (ctypes.c_int, [_DESC, _W, _P, _I32, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "pi_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "pi_selftest_wait_timeout": (ctypes.c_int, [_P, _P, _SZ, _I64, _P]),
+    "pi_pack_weights": (ctypes.c_int, [_DESC, _P, _P, _P, _P]),
 }
 
 
@@ -131,8 +133,9 @@ def check(status: int, where: str = "libpi") -> None:
 
 
 def make_desc(d: int, n: int, r: int, dtype: str = "f16", gated: bool = False,
-              hot_prefix: int = 0) -> pi_ffn_desc:
-    return pi_ffn_desc(d, n, r, PI_BF16 if dtype == "bf16" else PI_F16, int(gated), hot_prefix)
+              hot_prefix: int = 0, packed: bool = False) -> pi_ffn_desc:
+    return pi_ffn_desc(d, n, r, PI_BF16 if dtype == "bf16" else PI_F16, int(gated), hot_prefix,
+                       PI_LAYOUT_PACKED if packed else PI_LAYOUT_SPLIT)
 
 
 def make_weights(A, Bm, b1, W1, W2, b2=None) -> pi_layer_weights:
@@ -185,6 +188,11 @@ def pi_layer_decode(desc, w, x, batch, y, residual, idx_out, cnt_out, dev_status
     return lib().pi_layer_decode(ctypes.byref(desc), ctypes.byref(w), _ptr(x), batch, _ptr(y),
                                  _ptr(residual), _ptr(idx_out), _ptr(cnt_out), _ptr(dev_status),
                                  _ptr(ws), ws.numel() if ws_bytes is None else ws_bytes,
+                                 _stream(stream))
+
+
+def pi_pack_weights(desc, W1, W2, packed, stream=None) -> int:
+    return lib().pi_pack_weights(ctypes.byref(desc), _ptr(W1), _ptr(W2), _ptr(packed),
                                  _stream(stream))
 
 

@@ -9,8 +9,9 @@
 
 namespace pik {
 
-constexpr int kThreads = 512;             // block size of the persistent kernels
+constexpr int kThreads = 512;             // compute threads of a persistent block
 constexpr int kWarps = kThreads / 32;
+constexpr int kBlock = kThreads + 32;     // + one producer warp issuing TMA copies
 constexpr int kPMax = 512;                // largest persistent grid supported
 constexpr int kSMax = 8;                  // largest split of a predictor row
 constexpr int kMaxBatch = 32;
@@ -76,48 +77,168 @@ __device__ __forceinline__ void set_status(int* st, int code) {
   if (st) atomicCAS(st, 0, code);
 }
 
-// Barrier state in the workspace: arrival counter and generation word on
-// separate 128-byte lines.
-struct GridBar {
-  unsigned* count;
-  unsigned* gen;
-};
+__device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
 
-// Grid-wide barrier of `expected` blocks with a bounded wait.  Every block
-// must call it the same number of times.  Returns false (and records
-// PI_ERR_TIMEOUT) when the generation did not advance within limit_ns.
-// Writes made by the block before the call are visible to every block after
-// it (read them with ld.cg / __ldcg: L1 is not coherent across blocks).
-__device__ __noinline__ bool grid_sync(GridBar bar, unsigned expected, int* status,
-                                       uint64_t limit_ns) {
+// Grid-wide barriers on one 64-bit arrival counter in the workspace.  Each
+// barrier adds exactly one arrival per block, so at the start of a launch the
+// counter is a multiple of the grid size P; a block reads it once
+// (grid_base) and barrier k of the launch waits for base + k P arrivals.
+// Arrival is a fire-and-forget reduction (no round trip); the wait is
+// bounded by limit_ns and records PI_ERR_TIMEOUT when it runs out.  Writes
+// made by the block before the call are visible to every block after it
+// (read them with ld.cg / __ldcg: L1 is not coherent across blocks).
+__device__ __forceinline__ unsigned long long grid_base(const unsigned long long* ctr,
+                                                        unsigned nblocks) {
+  const unsigned long long v = ld_acquire64(ctr);
+  return v - v % nblocks;
+}
+
+__device__ __noinline__ bool grid_sync(unsigned long long* ctr, unsigned long long target,
+                                       int* status, uint64_t limit_ns) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
     int ok = 1;
-    const unsigned g = ld_acquire(bar.gen);
     __threadfence();
-    const unsigned prev = atomicAdd(bar.count, 1u);
-    if (prev == expected - 1u) {
-      atomicExch(bar.count, 0u);
-      __threadfence();
-      st_release(bar.gen, g + 1u);
-    } else {
-      const uint64_t t0 = global_ns();
-      unsigned spins = 0;
-      while (ld_acquire(bar.gen) == g) {
-        if ((++spins & 63u) == 0u && global_ns() - t0 > limit_ns) {
-          ok = 0;
-          set_status(status, PI_ERR_TIMEOUT);
-          break;
-        }
-        __nanosleep(20);
+    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(ctr) : "memory");
+    const uint64_t t0 = global_ns();
+    unsigned spins = 0;
+    while ((long long)(ld_acquire64(ctr) - target) < 0) {
+      if ((++spins & 15u) == 0u && global_ns() - t0 > limit_ns) {
+        ok = 0;
+        set_status(status, PI_ERR_TIMEOUT);
+        break;
       }
     }
-    __threadfence();
     s_ok = ok;
   }
   __syncthreads();
   return s_ok != 0;
+}
+
+// ------------------------------------------------------------------ TMA bulk copies
+__device__ __forceinline__ unsigned smem_u32(const void* p) {
+  return (unsigned)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* m, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(m)), "r"(count) : "memory");
+}
+
+// Barrier among the kThreads compute threads only (the producer warp keeps
+// running its own loop).
+__device__ __forceinline__ void compute_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+}
+
+// Makes mbarrier initialisation visible to the asynchronous (TMA) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* m) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(m)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* m, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(m)),
+               "r"(bytes)
+               : "memory");
+}
+
+// One-dimensional bulk copy global -> shared (TMA unit), completing on `m`.
+// Addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* sdst, const void* gsrc, unsigned bytes, uint64_t* m) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(sdst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(m))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* m, unsigned parity) {
+  unsigned ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(m)), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+
+// Non-blocking test of the phase of parity `parity`.
+__device__ __forceinline__ bool mbar_test(uint64_t* m, unsigned parity) {
+  unsigned ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(m)), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+
+// Waits for the phase of parity `parity` of `m` to complete; gives up after
+// limit_ns and returns false.  The common case (already complete) costs one
+// non-blocking test.
+__device__ __forceinline__ bool mbar_wait(uint64_t* m, unsigned parity, uint64_t limit_ns) {
+  if (mbar_test(m, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(m, parity))
+    if (global_ns() - t0 > limit_ns) return false;
+  return true;
+}
+
+// The same for a thread that only waits (the producer warp): sleeps between
+// polls so that it takes no issue slots from the compute warps.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* m, unsigned parity, uint64_t limit_ns) {
+  if (mbar_test(m, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(m, parity)) {
+    if (global_ns() - t0 > limit_ns) return false;
+    __nanosleep(64);
+  }
+  return true;
+}
+
+// Transposing butterfly reduction of NV values (NV a power of two, <= 32)
+// held by each lane of a warp: on return every lane holds the warp-wide sum
+// of value index bfly_index<NV>(lane).  NV - 1 + log2(32 / NV) shuffles
+// instead of 5 NV.
+template <int NV>
+__device__ __forceinline__ float warp_bfly_sum(float (&v)[NV]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int half = NV / 2, off = 16; half >= 1; half >>= 1, off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = upper ? v[i] : v[i + half];
+      const float keep = upper ? v[i + half] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  float r = v[0];
+#pragma unroll
+  for (int off = (32 / NV) / 2; off >= 1; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
+  return r;
+}
+
+template <int NV>
+__device__ __forceinline__ int bfly_index(int lane) {
+  int vi = 0;
+#pragma unroll
+  for (int half = NV / 2, off = 16; half >= 1; half >>= 1, off >>= 1)
+    if (lane & off) vi += half;
+  return vi;
 }
 
 }  // namespace pik

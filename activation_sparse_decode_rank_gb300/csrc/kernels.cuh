@@ -15,15 +15,25 @@ namespace pik {
 
 enum Mode { kFused = 0, kSparse = 1, kDense = 2 };
 
+constexpr int kGroup = 4;        // neurons per round
+constexpr int kMaxSlots = 16;    // TMA ring slots
+
 struct FfnArgs {
   int d, n, r;
-  int S;          // predictor row split (fused path)
-  int P;          // grid size (all blocks co-resident)
-  int hot;        // hot-prefix length (rows fetched into L2 up front)
-  int nch;        // d / 8: 16-byte column chunks of a row
-  int rows_max;   // ceil(n / P)
+  int S;           // predictor row split (fused path)
+  int P;           // grid size (all blocks co-resident)
+  int hot;         // hot-prefix length
+  int nch;         // d / 8: 16-byte column chunks of a row
+  int rows_max;    // most neurons a block lists (own neurons, or list positions)
+  int a_in_smem;   // fused: own predictor rows staged in shared memory (else read via L2)
+  int a_stride;    // bytes between staged predictor rows (2 r + 16: conflict-free reads)
+  int ns;          // ring slots (one neuron's W1 row(s) + W2 row each)
+  int nh;          // fused: slots [0, nh) take the block's own hot neurons up front
+  int grp;         // (unused: rounds hold kGroup neurons; needs ns - nh >= kGroup)
+  int slot_bytes;
+  int packed;      // PI_LAYOUT_PACKED: W1 holds [n][m d] per-neuron records
   // dynamic shared-memory offsets (bytes)
-  int o_xs, o_us, o_As, o_b1s, o_flag, o_lst, o_off, o_wl, o_red;
+  int o_xs, o_us, o_As, o_b1s, o_flag, o_lst, o_lb, o_off, o_red, o_mbar, o_slots;  // o_off unused
   const uint16_t* A;
   const uint16_t* Bm;
   const float* b1;
@@ -39,11 +49,11 @@ struct FfnArgs {
   int* idx_out;
   int* cnt_out;
   int* status;
-  GridBar bar;
-  float* upart;   // [r * S]
-  int* loc_cnt;   // [P]
-  int* loc_idx;   // [n]
-  float* part;    // [P][d]
+  unsigned long long* bar;  // grid barrier arrival counter
+  float* upart;             // [r * S]
+  int* loc_tot;             // [P] active count of each block's own neurons
+  unsigned char* mask;      // [n] predicted mask (only when idx_out is wanted)
+  float* part;              // [P][d]
   unsigned long long limit_ns;
 };
 
@@ -77,206 +87,262 @@ __device__ __forceinline__ float dot8(const float f[8], const float x[8]) {
   return s;
 }
 
-// ------------------------------------------------------------ predictor
-// Stage 1 of the fused path: the r x S units (row k of Bm, column segment s)
-// are spread over the grid; unit q's partial dot product goes to upart[q].
-template <int DT>
-__device__ void fused_u(const FfnArgs& a, const float* xs, float* red) {
-  const int c = blockIdx.x;
-  const int units = a.r * a.S;
-  const int seg = a.d / a.S;
-  const int segc = seg >> 3;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int q0 = c; q0 < units; q0 += 4 * a.P) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int uu = 0; uu < 4; ++uu) {
-      const int q = q0 + uu * a.P;
-      if (q < units) {
-        const int k = q / a.S, s = q - k * a.S;
-        const uint16_t* row = a.Bm + (size_t)k * a.d + (size_t)s * seg;
-        const float* xp = xs + (size_t)s * seg;
-        for (int ch = threadIdx.x; ch < segc; ch += kThreads) {
-          float f[8], xv[8];
-          unpack8<DT>(ld_nc(row + 8 * ch), f);
-          const float4 x0 = *reinterpret_cast<const float4*>(xp + 8 * ch);
-          const float4 x1 = *reinterpret_cast<const float4*>(xp + 8 * ch + 4);
-          xv[0] = x0.x; xv[1] = x0.y; xv[2] = x0.z; xv[3] = x0.w;
-          xv[4] = x1.x; xv[5] = x1.y; xv[6] = x1.z; xv[7] = x1.w;
-          acc[uu] += dot8(f, xv);
-        }
-      }
-    }
-#pragma unroll
-    for (int uu = 0; uu < 4; ++uu) acc[uu] = warp_sum(acc[uu]);
-    if (lane == 0) {
-#pragma unroll
-      for (int uu = 0; uu < 4; ++uu) red[warp * 4 + uu] = acc[uu];
-    }
-    __syncthreads();
-    if (threadIdx.x < 4) {
-      const int q = q0 + threadIdx.x * a.P;
-      if (q < units) {
-        float s = 0.f;
-        for (int w = 0; w < kWarps; ++w) s += red[w * 4 + threadIdx.x];
-        __stcg(a.upart + q, s);
-      }
-    }
-    __syncthreads();
+__device__ __forceinline__ void load8(const float* p, float v[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+// Arms ring slot `slot` with neuron `i`: its W1 row (gated: gate and up rows)
+// and its W2 row, by bulk copies completing on the slot's "full" mbarrier.
+// A slot holds [W1 part | W2 part], the byte layout of a packed record, so a
+// packed layer needs one copy per neuron, a split one two.
+template <bool GATED>
+__device__ __forceinline__ void issue_neuron(const FfnArgs& a, unsigned char* slots, uint64_t* full,
+                                             int slot, int i) {
+  unsigned char* dst = slots + (size_t)slot * a.slot_bytes;
+  mbar_expect_tx(full + slot, (unsigned)a.slot_bytes);
+  if (a.packed) {
+    bulk_g2s(dst, reinterpret_cast<const unsigned char*>(a.W1) + (size_t)i * a.slot_bytes,
+             (unsigned)a.slot_bytes, full + slot);
+  } else {
+    const unsigned w1b = (GATED ? 4u : 2u) * (unsigned)a.d;
+    const size_t rs = GATED ? 2 * (size_t)a.d : (size_t)a.d;
+    bulk_g2s(dst, a.W1 + (size_t)i * rs, w1b, full + slot);
+    bulk_g2s(dst + w1b, a.W2 + (size_t)i * a.d, 2u * (unsigned)a.d, full + slot);
   }
 }
 
-// Stage 2 of the fused path: logits of this block's neuron slice from the
-// A rows staged in shared memory; flag[row] = (logit > 0).
+// Asks L2 to fetch neuron i's rows (no completion; used for hot neurons
+// that do not fit the ring).
+template <bool GATED>
+__device__ __forceinline__ void prefetch_neuron(const FfnArgs& a, int i) {
+  if (a.packed) {
+    prefetch_l2(reinterpret_cast<const unsigned char*>(a.W1) + (size_t)i * a.slot_bytes,
+                (unsigned long long)a.slot_bytes);
+  } else {
+    const size_t rs = GATED ? 2 * (size_t)a.d : (size_t)a.d;
+    prefetch_l2(a.W1 + (size_t)i * rs, rs * 2);
+    prefetch_l2(a.W2 + (size_t)i * a.d, (size_t)a.d * 2);
+  }
+}
+
+// ------------------------------------------------------------ predictor (fused)
+// Logits of this block's own neurons i = c + j P (j < rows), four lanes per
+// row, eight rows per warp at a time; flag[j] = (logit > 0).
 template <int DT>
-__device__ void fused_logits(const FfnArgs& a, const uint16_t* As, const float* b1s,
-                             const float* us, int* flag, int rows) {
+__device__ void own_logits(const FfnArgs& a, const unsigned char* As, const float* b1s,
+                           const float* us, unsigned char* flag, int rows) {
   const int rc = a.r >> 3;
-  int G = 1;
-  while (G < rc) G <<= 1;
-  const int RPW = 32 / G;
+  const int c = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane / G, l = lane - g * G;
-  float uf[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) uf[e] = (l < rc) ? us[8 * l + e] : 0.f;
-  for (int base = warp * RPW; base < rows; base += kWarps * RPW) {
-    const int row = base + g;
+  const int g = lane >> 2, l = lane & 3;
+  for (int base = warp * 8; base < rows; base += kWarps * 8) {
+    const int j = base + g;
     float acc = 0.f;
-    if (row < rows && l < rc) {
-      float f[8];
-      unpack8<DT>(*reinterpret_cast<const uint4*>(As + (size_t)row * a.r + 8 * l), f);
-      acc = dot8(f, uf);
+    if (j < rows) {
+      for (int q = l; q < rc; q += 4) {
+        uint4 v;
+        if (a.a_in_smem)
+          v = *reinterpret_cast<const uint4*>(As + (size_t)j * a.a_stride + 16 * q);
+        else
+          v = ld_nc(a.A + ((size_t)c + (size_t)j * a.P) * a.r + 8 * q);
+        float f[8], u[8];
+        unpack8<DT>(v, f);
+        load8(us + 8 * q, u);
+        acc += dot8(f, u);
+      }
     }
-    for (int o = G >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (row < rows && l == 0) flag[row] = (acc + b1s[row] > 0.f) ? 1 : 0;
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    if (j < rows && l == 0) flag[j] = (acc + b1s[j] > 0.f) ? 1 : 0;
   }
 }
 
-// ------------------------------------------------------------ FFN rows
-// Row-gather GEMV + ReLU and row-axpy over the m neurons listed in wl.
-// Thread t owns the 16-byte column chunks t, t + kThreads, ... of every row;
-// KC neurons are in flight at a time (all their W1 and W2 loads issued
-// before any is used).  The per-neuron dot products are reduced across the
-// block in a fixed order, so the result is deterministic.
-template <int DT, bool GATED, int NCH, int KC>
-__device__ void ffn_rows(const FfnArgs& a, const float* xs, const int* wl, int m, float* red,
-                         float (&yacc)[NCH][8]) {
+// ------------------------------------------------------------ FFN over a neuron list
+// Row-gather GEMV + ReLU and row-axpy over the m neurons of lst.  Rows reach
+// shared memory by TMA bulk copies.  Entries [0, mh) are the block's own hot
+// neurons, armed up front into slots (lst[k] - c) / P; the other entries
+// cycle through slots [nh, ns), armed by the producer warp as soon as the
+// compute warps release a slot ("empty" mbarrier, one arrival per compute
+// warp).  Compute thread t owns the 16-byte column chunks t, t + kThreads,
+// ... of every row and keeps x of those columns in registers.  Work goes in
+// rounds of up to kGroup neurons:
+//   A. each thread dots its chunks of the round's W1 rows with x; one
+//      transposing butterfly per warp reduces all of them; warp partials go
+//      to shared memory;
+//   B. eight lanes of warp 0 add the kWarps partials in order, add the bias
+//      and apply ReLU (times the up projection, gated);
+//   C. each thread adds h_q times its chunks of the round's W2 rows.
+// Every sum has a fixed order, so results are deterministic.  Needs kGroup
+// <= ns - nh (no round waits for a slot that only its own release would
+// free).  lb[k] is b1 of neuron lst[k]; red holds 2 x kGroup x NV x kWarps
+// floats, hbuf 2 x kGroup.
+template <int DT, bool GATED, int NCH>
+__device__ void ffn_ring(const FfnArgs& a, const float* xs, const int* lst, const float* lb, int m,
+                         int mh, int nh, unsigned char* slots, uint64_t* full, uint64_t* empty,
+                         float* red, float* hbuf, float (&yacc)[NCH][8], int* bad) {
   constexpr int NV = GATED ? 2 : 1;
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const size_t rs = GATED ? 2 * (size_t)a.d : (size_t)a.d;
+  constexpr int NR = kGroup * NV;  // values reduced per round
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c = blockIdx.x;
+  const int nc = a.ns - nh;
+  const int mc = m - mh;
+  if (warp == kWarps) {  // producer warp
+    if (lane == 0) {
+      for (int kc = 0; kc < mc; ++kc) {
+        const int s = nh + kc % nc;
+        if (kc >= nc &&
+            !mbar_wait_sleep(empty + s, (unsigned)((kc / nc - 1) & 1), a.limit_ns)) {
+          set_status(a.status, PI_ERR_TIMEOUT);
+          *bad = 1;
+          break;
+        }
+        issue_neuron<GATED>(a, slots, full, s, lst[mh + kc]);
+      }
+    }
+    return;
+  }
+  const unsigned w1b = (GATED ? 4u : 2u) * (unsigned)a.d;
   float xr[NCH][8];
   bool colok[NCH];
 #pragma unroll
   for (int j = 0; j < NCH; ++j) {
-    const int cc = t + j * kThreads;
+    const int cc = tid + j * kThreads;
     colok[j] = cc < a.nch;
 #pragma unroll
     for (int e = 0; e < 8; ++e) xr[j][e] = colok[j] ? xs[8 * cc + e] : 0.f;
   }
+  int cslot = 0, cpar = 0;  // ring position of the next cold entry
   int buf = 0;
-  for (int base = 0; base < m; base += KC) {
-    const int kc = min(KC, m - base);
-    int nk[KC];
-    float bk[KC];
+  for (int g0 = 0; g0 < m; g0 += kGroup) {
+    const int kg = min(kGroup, m - g0);
+    int sl[kGroup];
 #pragma unroll
-    for (int k = 0; k < KC; ++k) nk[k] = (k < kc) ? wl[base + k] : -1;
-#pragma unroll
-    for (int k = 0; k < KC; ++k) bk[k] = (nk[k] >= 0) ? __ldg(a.b1 + nk[k]) : 0.f;
-    uint4 w1[KC][NCH], wu[GATED ? KC : 1][NCH], w2[KC][NCH];
-#pragma unroll
-    for (int k = 0; k < KC; ++k) {
-#pragma unroll
-      for (int j = 0; j < NCH; ++j) {
-        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-        w1[k][j] = z;
-        w2[k][j] = z;
-        if (GATED) wu[GATED ? k : 0][j] = z;
-        if (nk[k] >= 0 && colok[j]) {
-          const size_t col = 8 * (size_t)(t + j * kThreads);
-          const size_t nrow = (size_t)nk[k];
-          w1[k][j] = ld_stream(a.W1 + nrow * rs + col);
-          if (GATED) wu[GATED ? k : 0][j] = ld_stream(a.W1 + nrow * rs + a.d + col);
-          w2[k][j] = ld_stream(a.W2 + nrow * (size_t)a.d + col);
+    for (int q = 0; q < kGroup; ++q) {
+      sl[q] = 0;
+      if (q < kg) {
+        const int k = g0 + q;
+        unsigned par = 0u;
+        if (k < mh) {
+          sl[q] = (lst[k] - c) / a.P;
+        } else {
+          sl[q] = nh + cslot;
+          par = (unsigned)cpar;
+          if (++cslot == nc) {
+            cslot = 0;
+            cpar ^= 1;
+          }
+        }
+        if (!mbar_wait(full + sl[q], par, a.limit_ns)) {
+          set_status(a.status, PI_ERR_TIMEOUT);
+          *bad = 1;
         }
       }
     }
-    float pd[KC][NV];
+    // A: partial dot products of the round, one butterfly per warp
+    float pd[NR];
 #pragma unroll
-    for (int k = 0; k < KC; ++k) {
+    for (int q = 0; q < kGroup; ++q) {
       float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-      for (int j = 0; j < NCH; ++j) {
-        float f[8];
-        unpack8<DT>(w1[k][j], f);
-        s0 += dot8(f, xr[j]);
-        if (GATED) {
-          unpack8<DT>(wu[GATED ? k : 0][j], f);
-          s1 += dot8(f, xr[j]);
-        }
-      }
-      pd[k][0] = warp_sum(s0);
-      if (GATED) pd[k][NV - 1] = warp_sum(s1);
-    }
-    float* rb = red + buf * (kWarps * KC * NV);
-    if (lane == 0) {
-#pragma unroll
-      for (int k = 0; k < KC; ++k)
-#pragma unroll
-        for (int v = 0; v < NV; ++v) rb[(warp * KC + k) * NV + v] = pd[k][v];
-    }
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < KC; ++k) {
-      if (k < kc) {
-        float s0 = 0.f, s1 = 0.f;
-        for (int w = 0; w < kWarps; ++w) {
-          s0 += rb[(w * KC + k) * NV];
-          if (GATED) s1 += rb[(w * KC + k) * NV + NV - 1];
-        }
-        float h = s0 + bk[k];
-        h = h > 0.f ? h : 0.f;  // ReLU; ReLU(0) = 0
-        if (GATED) h *= s1;
+      if (q < kg) {
+        const unsigned char* sp = slots + (size_t)sl[q] * a.slot_bytes;
 #pragma unroll
         for (int j = 0; j < NCH; ++j) {
-          float f[8];
-          unpack8<DT>(w2[k][j], f);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) yacc[j][e] = fmaf(h, f[e], yacc[j][e]);
+          if (colok[j]) {
+            const int cc = tid + j * kThreads;
+            float f[8];
+            unpack8<DT>(*reinterpret_cast<const uint4*>(sp + 16 * cc), f);
+            s0 += dot8(f, xr[j]);
+            if (GATED) {
+              unpack8<DT>(*reinterpret_cast<const uint4*>(sp + 2 * a.d + 16 * cc), f);
+              s1 += dot8(f, xr[j]);
+            }
+          }
         }
       }
+      pd[q * NV] = s0;
+      if (GATED) pd[q * NV + NV - 1] = s1;
+    }
+    const float r = warp_bfly_sum<NR>(pd);
+    float* rb = red + buf * (NR * kWarps);
+    if ((lane & (32 / NR - 1)) == 0) rb[bfly_index<NR>(lane) * kWarps + warp] = r;
+    compute_sync();
+    // B: h of the round's neurons
+    float* hb = hbuf + buf * kGroup;
+    if (warp == 0 && lane < kg) {
+      float s0 = 0.f, s1 = 0.f;
+      for (int w = 0; w < kWarps; ++w) {
+        s0 += rb[(lane * NV) * kWarps + w];
+        if (GATED) s1 += rb[(lane * NV + NV - 1) * kWarps + w];
+      }
+      float h = s0 + lb[g0 + lane];
+      h = h > 0.f ? h : 0.f;  // ReLU; ReLU(0) = 0
+      if (GATED) h *= s1;
+      hb[lane] = h;
+    }
+    compute_sync();
+    // C: row-axpy of the round's W2 rows
+#pragma unroll
+    for (int q = 0; q < kGroup; ++q) {
+      if (q < kg) {
+        const float h = hb[q];
+        const unsigned char* sp = slots + (size_t)sl[q] * a.slot_bytes + w1b;
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+          if (colok[j]) {
+            const int cc = tid + j * kThreads;
+            float f[8];
+            unpack8<DT>(*reinterpret_cast<const uint4*>(sp + 16 * cc), f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) yacc[j][e] = fmaf(h, f[e], yacc[j][e]);
+          }
+        }
+      }
+    }
+    // this warp is done with the round's slots: release the recycled ones
+    __syncwarp();
+    if (lane == 0) {
+#pragma unroll
+      for (int q = 0; q < kGroup; ++q)
+        if (q < kg && g0 + q >= mh) mbar_arrive(empty + sl[q]);
     }
     buf ^= 1;
   }
 }
 
-// Sums the P partial rows in ascending block order (fixed split over
-// threads), adds b2 and the residual, writes y.  Block c owns a slice of
-// the d/4 float4 columns.
-__device__ void final_reduce(const FfnArgs& a, float4* red4) {
+// Sums the P partial rows in a fixed order, adds b2 and the residual, writes
+// y.  Block c owns a slice of the d/4 float4 columns, one column per compute
+// warp at a time: lane l sums partials l, l + 32, l + 64, ... (all loads
+// issued first), then the 32 lane sums meet in a fixed shuffle tree.
+__device__ void final_reduce(const FfnArgs& a) {
   const int c = blockIdx.x, P = a.P;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int D4 = a.d >> 2;
   const int j0 = (int)((long long)c * D4 / P), j1 = (int)((long long)(c + 1) * D4 / P);
-  constexpr int JB = 8, Q = kThreads / JB;
-  const int jl = threadIdx.x % JB, q = threadIdx.x / JB;
-  const int p0 = q * P / Q, p1 = (q + 1) * P / Q;
-  for (int jb = j0; jb < j1; jb += JB) {
-    const int j = jb + jl;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (j < j1) {
-      for (int p = p0; p < p1; ++p) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)p * a.d) + j);
-        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-      }
+  constexpr int PU = kPMax / 32;
+  for (int j = j0 + warp; j < j1; j += kWarps) {
+    float4 v[PU];
+#pragma unroll
+    for (int u = 0; u < PU; ++u) {
+      const int p = lane + 32 * u;
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (p < P) v[u] = __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)p * a.d) + j);
     }
-    red4[q * JB + jl] = acc;
-    __syncthreads();
-    if (q == 0 && j < j1) {
-      float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int qq = 0; qq < Q; ++qq) {
-        const float4 v = red4[qq * JB + jl];
-        s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
-      }
+    float4 s = v[0];
+#pragma unroll
+    for (int u = 1; u < PU; ++u) {
+      s.x += v[u].x; s.y += v[u].y; s.z += v[u].z; s.w += v[u].w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      s.x += __shfl_xor_sync(0xffffffffu, s.x, o);
+      s.y += __shfl_xor_sync(0xffffffffu, s.y, o);
+      s.z += __shfl_xor_sync(0xffffffffu, s.z, o);
+      s.w += __shfl_xor_sync(0xffffffffu, s.w, o);
+    }
+    if (lane == 0) {
       if (a.b2) {
         const float4 b = __ldg(reinterpret_cast<const float4*>(a.b2) + j);
         s.x += b.x; s.y += b.y; s.z += b.z; s.w += b.w;
@@ -287,138 +353,242 @@ __device__ void final_reduce(const FfnArgs& a, float4* red4) {
       }
       reinterpret_cast<float4*>(a.y)[j] = s;
     }
-    __syncthreads();
+  }
+}
+
+// Ascending active list of the whole layer from the predicted mask: block c
+// compacts mask[c n/P, (c+1) n/P), offset by the number of active neurons
+// below its range.  Compute threads only.
+__device__ void write_active_list(const FfnArgs& a, int* red_i) {
+  const int c = blockIdx.x, P = a.P;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int lo = (int)((long long)c * a.n / P), hi = (int)((long long)(c + 1) * a.n / P);
+  int below = 0;
+  const int lo16 = lo & ~15;
+  for (int e = tid * 16; e < lo16; e += kThreads * 16) {
+    const uint4 v = __ldcg(reinterpret_cast<const uint4*>(a.mask + e));
+    below += __popc(v.x) + __popc(v.y) + __popc(v.z) + __popc(v.w);  // bytes are 0 or 1
+  }
+  if (tid < lo - lo16) below += __ldcg(a.mask + lo16 + tid);
+  below = __reduce_add_sync(0xffffffffu, below);
+  if (lane == 0) red_i[warp] = below;
+  compute_sync();
+  if (warp == 0) {
+    int base = 0;
+    for (int w = 0; w < kWarps; ++w) base += red_i[w];
+    for (int b0 = lo; b0 < hi; b0 += 32) {
+      const int i = b0 + lane;
+      const bool f = (i < hi) && __ldcg(a.mask + i);
+      const unsigned bal = __ballot_sync(0xffffffffu, f);
+      if (f) a.idx_out[base + __popc(bal & ((1u << lane) - 1u))] = i;
+      base += __popc(bal);
+    }
   }
 }
 
 // ------------------------------------------------------------ persistent FFN kernel
-// MODE kFused : predictor + compaction + sparse FFN of one token (one launch)
-// MODE kSparse: sparse FFN over a given active list (idx_in, cnt_in)
-// MODE kDense : FFN over all n neurons
-// All P blocks must be co-resident (cooperative launch); the grid-wide waits
-// are bounded by limit_ns.
-template <int DT, bool GATED, int NCH, int KC, int MODE>
-__global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const FfnArgs a) {
-  extern __shared__ __align__(16) unsigned char smem[];
+// MODE kFused : predictor + mask + sparse FFN of one token (one launch).
+//               Block c owns neurons c, c + P, c + 2P, ... (interleaving
+//               spreads the hot prefix evenly), scores them and computes its
+//               active ones; the rows of its first hot neurons were fetched
+//               into shared memory before the mask was known.  Two grid-wide
+//               waits: the predictor's u and the final split reduction.  The
+//               per-block active counts vary, but with whole-neuron bulk
+//               copies the chip's bandwidth, not one block, bounds the time.
+// MODE kSparse: sparse FFN over a given active list (idx_in, cnt_in), split
+//               evenly over the blocks.
+// MODE kDense : FFN over all n neurons.
+// kThreads compute threads + one producer warp per block; all P blocks
+// must be co-resident (cooperative launch); every wait is bounded.
+template <int DT, bool GATED, int NCH, int MODE>
+__global__ void __launch_bounds__(kBlock, 1) ffn_kernel(const FfnArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
   float* xs = reinterpret_cast<float*>(smem + a.o_xs);
-  int* wl = reinterpret_cast<int*>(smem + a.o_wl);
+  int* lst = reinterpret_cast<int*>(smem + a.o_lst);
+  float* lb = reinterpret_cast<float*>(smem + a.o_lb);
   float* red = reinterpret_cast<float*>(smem + a.o_red);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.o_mbar);
+  uint64_t* empty = full + kMaxSlots;
+  unsigned char* slots = smem + a.o_slots;
   const int c = blockIdx.x, P = a.P;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int m = 0;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool compute = tid < kThreads;
+  __shared__ int s_m, s_mh, s_bad;
+  __shared__ unsigned long long s_base;
+
+  const int hot_own = (MODE == kFused && c < a.hot) ? (a.hot - 1 - c) / P + 1 : 0;
+  const int nh = (MODE == kFused) ? a.nh : 0;
+  const int nh_c = min(nh, hot_own);  // own hot neurons whose rows go to slots up front
+  if (tid == 0) {
+    for (int s = 0; s < a.ns; ++s) {
+      mbar_init(full + s, 1u);
+      mbar_init(empty + s, (unsigned)kWarps);
+    }
+    fence_mbar_init();
+    // weights that do not depend on x go out first: own hot neurons' rows
+    for (int j = 0; j < nh_c; ++j) issue_neuron<GATED>(a, slots, full, j, c + j * P);
+    s_bad = 0;
+    s_base = grid_base(a.bar, (unsigned)P);
+  }
+  int m = 0, mh = 0;
 
   if (MODE == kFused) {
-    const int lo = (int)((long long)c * a.n / P), hi = (int)((long long)(c + 1) * a.n / P);
-    const int rows = hi - lo;
-    uint16_t* As = reinterpret_cast<uint16_t*>(smem + a.o_As);
+    const int rows = (c < a.n) ? (a.n - 1 - c) / P + 1 : 0;  // own neurons
+    unsigned char* As = smem + a.o_As;
     float* b1s = reinterpret_cast<float*>(smem + a.o_b1s);
     float* us = reinterpret_cast<float*>(smem + a.o_us);
-    int* flag = reinterpret_cast<int*>(smem + a.o_flag);
-    int* lst = reinterpret_cast<int*>(smem + a.o_lst);
+    unsigned char* flag = smem + a.o_flag;
     int* off = reinterpret_cast<int*>(smem + a.o_off);
-    __shared__ int s_cnt;
+    const int units = a.r * a.S;
+    const int seg = a.d / a.S;
+    const int segc = seg >> 3;
 
-    // The predictor's A rows and biases of this slice do not depend on x:
-    // start fetching them now, behind stage 1.
-    {
-      const char* src = reinterpret_cast<const char*>(a.A + (size_t)lo * a.r);
-      const int bytes = rows * a.r * 2;
-      for (int o = threadIdx.x * 16; o < bytes; o += kThreads * 16)
-        cp_async16(reinterpret_cast<char*>(As) + o, src + o);
-      for (int i = threadIdx.x; i < rows; i += kThreads) cp_async4(b1s + i, a.b1 + lo + i);
-      cp_async_commit();
+    // 1. x first: it is the latency-critical input
+    float4 xv4[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const int i = tid + h * kThreads;
+      xv4[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (compute && i < (a.d >> 2)) xv4[h] = __ldg(reinterpret_cast<const float4*>(a.x) + i);
     }
-    // Hot block: bring this block's share of the hot rows of W1 and W2
-    // towards the chip before the mask is known.
-    if (a.hot > 0 && threadIdx.x == 0) {
-      const int h0 = (int)((long long)c * a.hot / P), h1 = (int)((long long)(c + 1) * a.hot / P);
-      if (h1 > h0) {
-        const size_t rs = GATED ? 2 * (size_t)a.d : (size_t)a.d;
-        prefetch_l2(a.W1 + (size_t)h0 * rs, (unsigned long long)(h1 - h0) * rs * 2);
-        prefetch_l2(a.W2 + (size_t)h0 * a.d, (unsigned long long)(h1 - h0) * a.d * 2);
+    // 2. this block's first predictor-stage-1 units (Bm chunks)
+    uint4 bw[2][2];
+#pragma unroll
+    for (int uu = 0; uu < 2; ++uu) {
+      const int q = c + uu * P;
+      const int k = q / a.S, s = q - k * a.S;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int ch = tid + h * kThreads;
+        bw[uu][h] = make_uint4(0u, 0u, 0u, 0u);
+        if (compute && q < units && ch < segc)
+          bw[uu][h] = ld_nc(a.Bm + (size_t)k * a.d + (size_t)s * seg + 8 * ch);
       }
     }
-    for (int i = threadIdx.x; i < (a.d >> 2); i += kThreads)
-      reinterpret_cast<float4*>(xs)[i] = __ldg(reinterpret_cast<const float4*>(a.x) + i);
+    // 3. more weights that do not depend on x: the own hot neurons beyond
+    //    the slots towards L2, the own predictor rows and biases
+    if (compute) {
+      for (int j = nh_c + tid; j < hot_own; j += kThreads) prefetch_neuron<GATED>(a, c + j * P);
+      const int rc = a.r >> 3;
+      if (a.a_in_smem) {
+        for (int e = tid; e < rows * rc; e += kThreads) {
+          const int j = e / rc, q = e - j * rc;
+          cp_async16(As + (size_t)j * a.a_stride + 16 * q,
+                     a.A + ((size_t)c + (size_t)j * P) * a.r + 8 * q);
+        }
+      } else {
+        for (int j = tid; j < rows; j += kThreads)
+          prefetch_l2(a.A + ((size_t)c + (size_t)j * P) * a.r, (size_t)a.r * 2);
+      }
+      for (int j = tid; j < rows; j += kThreads) cp_async4(b1s + j, a.b1 + c + (size_t)j * P);
+      cp_async_commit();
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const int i = tid + h * kThreads;
+        if (i < (a.d >> 2)) reinterpret_cast<float4*>(xs)[i] = xv4[h];
+      }
+    }
     __syncthreads();
-
-    fused_u<DT>(a, xs, red);
-    if (!grid_sync(a.bar, (unsigned)P, a.status, a.limit_ns)) {
+    // 4. predictor stage 1: partial dot products of the units
+    for (int q0 = c; q0 < units; q0 += 2 * P) {
+      if (q0 != c) {
+#pragma unroll
+        for (int uu = 0; uu < 2; ++uu) {
+          const int q = q0 + uu * P;
+          const int k = q / a.S, s = q - k * a.S;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int ch = tid + h * kThreads;
+            bw[uu][h] = make_uint4(0u, 0u, 0u, 0u);
+            if (compute && q < units && ch < segc)
+              bw[uu][h] = ld_nc(a.Bm + (size_t)k * a.d + (size_t)s * seg + 8 * ch);
+          }
+        }
+      }
+      float acc[2] = {0.f, 0.f};
+#pragma unroll
+      for (int uu = 0; uu < 2; ++uu) {
+        const int q = q0 + uu * P;
+        const int s = q - (q / a.S) * a.S;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int ch = tid + h * kThreads;
+          if (compute && q < units && ch < segc) {
+            float f[8], xv[8];
+            unpack8<DT>(bw[uu][h], f);
+            load8(xs + (size_t)s * seg + 8 * ch, xv);
+            acc[uu] += dot8(f, xv);
+          }
+        }
+      }
+#pragma unroll
+      for (int uu = 0; uu < 2; ++uu) acc[uu] = warp_sum(acc[uu]);
+      if (compute && lane == 0) {
+        red[warp * 2] = acc[0];
+        red[warp * 2 + 1] = acc[1];
+      }
+      __syncthreads();
+      if (tid < 2) {
+        const int q = q0 + tid * P;
+        if (q < units) {
+          float sum = 0.f;
+          for (int w = 0; w < kWarps; ++w) sum += red[w * 2 + tid];
+          __stcg(a.upart + q, sum);
+        }
+      }
+      __syncthreads();
+    }
+    if (!grid_sync(a.bar, s_base + (unsigned long long)P, a.status, a.limit_ns)) {
       cp_async_wait_all();
+      if (tid == kThreads)
+        for (int j = 0; j < nh_c; ++j) mbar_wait(full + j, 0u, a.limit_ns);
+      __syncthreads();
       return;
     }
-    for (int k = threadIdx.x; k < a.r; k += kThreads) {
-      float s = 0.f;
-      for (int ss = 0; ss < a.S; ++ss) s += __ldcg(a.upart + k * a.S + ss);
-      us[k] = s;
+    // 5. u, logits of the own neurons, mask
+    for (int k = tid; k < a.r; k += kBlock) {
+      float sum = 0.f;
+      for (int ss = 0; ss < a.S; ++ss) sum += __ldcg(a.upart + k * a.S + ss);
+      us[k] = sum;
     }
     cp_async_wait_all();
     __syncthreads();
-    fused_logits<DT>(a, As, b1s, us, flag, rows);
+    if (compute) own_logits<DT>(a, As, b1s, us, flag, rows);
     __syncthreads();
-    // ordered compaction of this slice: ballot + popc, one warp
+    // 6. ordered list of the own active neurons (ballot + popc, one warp);
+    //    the hot ones whose rows sit in slots come first
     if (warp == 0) {
-      int cnt = 0;
+      int cnt = 0, nhot = 0;
       for (int base = 0; base < rows; base += 32) {
-        const int i = base + lane;
-        const bool f = (i < rows) && flag[i];
+        const int j = base + lane;
+        const bool f = (j < rows) && flag[j];
         const unsigned bal = __ballot_sync(0xffffffffu, f);
         const int pos = cnt + __popc(bal & ((1u << lane) - 1u));
         if (f) {
-          lst[pos] = lo + i;
-          __stcg(a.loc_idx + lo + pos, lo + i);
+          lst[pos] = c + j * P;
+          lb[pos] = b1s[j];
         }
+        if (a.mask && j < rows) a.mask[(size_t)c + (size_t)j * P] = f ? 1 : 0;
         cnt += __popc(bal);
+        nhot += __popc(__ballot_sync(0xffffffffu, f && j < nh_c));
       }
       if (lane == 0) {
-        s_cnt = cnt;
-        __stcg(a.loc_cnt + c, cnt);
-      }
-    }
-    if (!grid_sync(a.bar, (unsigned)P, a.status, a.limit_ns)) return;
-    // exclusive scan of the P slice counts (one warp)
-    if (warp == 0) {
-      int run = 0;
-      if (lane == 0) off[0] = 0;
-      for (int base = 0; base < P; base += 32) {
-        const int b = base + lane;
-        int v = (b < P) ? __ldcg(a.loc_cnt + b) : 0;
-        int incl = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int u = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += u;
-        }
-        if (b < P) off[b + 1] = run + incl;
-        run += __shfl_sync(0xffffffffu, incl, 31);
+        s_m = cnt;
+        s_mh = nhot;
+        __stcg(a.loc_tot + c, cnt);
       }
     }
     __syncthreads();
-    const int total = off[P];
-    if (a.idx_out)
-      for (int k = threadIdx.x; k < s_cnt; k += kThreads) a.idx_out[off[c] + k] = lst[k];
-    if (a.cnt_out && c == 0 && threadIdx.x == 0) a.cnt_out[0] = total;
-    // even split of the global active list over the grid
-    const long long p0 = (long long)c * total / P, p1 = (long long)(c + 1) * total / P;
-    m = (int)(p1 - p0);
-    for (int k = threadIdx.x; k < m; k += kThreads) {
-      const int p = (int)(p0 + k);
-      int lo_b = 0, hi_b = P - 1;  // largest b with off[b] <= p
-      while (lo_b < hi_b) {
-        const int mid = (lo_b + hi_b + 1) >> 1;
-        if (off[mid] <= p) lo_b = mid; else hi_b = mid - 1;
-      }
-      const int slo = (int)((long long)lo_b * a.n / P);
-      wl[k] = __ldcg(a.loc_idx + slo + (p - off[lo_b]));
-    }
+    m = s_m;
+    mh = s_mh;
   } else {
-    for (int i = threadIdx.x; i < (a.d >> 2); i += kThreads)
+    for (int i = tid; i < (a.d >> 2); i += kBlock)
       reinterpret_cast<float4*>(xs)[i] = __ldg(reinterpret_cast<const float4*>(a.x) + i);
     int total;
     if (MODE == kSparse) {
       total = __ldg(a.cnt_in);
       if (total < 0 || total > a.cap || total > a.n) {
-        if (c == 0 && threadIdx.x == 0) set_status(a.status, PI_ERR_CAPACITY);
+        if (c == 0 && tid == 0) set_status(a.status, PI_ERR_CAPACITY);
         return;  // uniform over the grid: no block reaches a grid-wide wait
       }
     } else {
@@ -426,35 +596,89 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_kernel(const FfnArgs a) {
     }
     const long long p0 = (long long)c * total / P, p1 = (long long)(c + 1) * total / P;
     m = (int)(p1 - p0);
-    for (int k = threadIdx.x; k < m; k += kThreads) {
+    for (int k = tid; k < m; k += kBlock) {
       int v = (MODE == kSparse) ? __ldg(a.idx_in + p0 + k) : (int)(p0 + k);
       if ((unsigned)v >= (unsigned)a.n) {  // never read outside the matrices
         set_status(a.status, PI_ERR_INDEX);
         v = -1;
       }
-      wl[k] = v;
+      lst[k] = v;
     }
+    __syncthreads();
+    // drop rejected entries, keeping the order
+    if (MODE == kSparse && warp == 0) {
+      int w = 0;
+      for (int base = 0; base < m; base += 32) {
+        const int k = base + lane;
+        const int v = (k < m) ? lst[k] : -1;
+        const unsigned bal = __ballot_sync(0xffffffffu, v >= 0);
+        __syncwarp();
+        if (v >= 0) lst[w + __popc(bal & ((1u << lane) - 1u))] = v;
+        __syncwarp();
+        w += __popc(bal);
+      }
+      if (lane == 0) s_m = w;
+    }
+    __syncthreads();
+    if (MODE == kSparse) m = s_m;
+    for (int k = tid; k < m; k += kBlock) lb[k] = __ldg(a.b1 + lst[k]);
+    __syncthreads();
   }
-  __syncthreads();
 
   float yacc[NCH][8];
 #pragma unroll
   for (int j = 0; j < NCH; ++j)
 #pragma unroll
     for (int e = 0; e < 8; ++e) yacc[j][e] = 0.f;
-  ffn_rows<DT, GATED, NCH, KC>(a, xs, wl, m, red, yacc);
-
-#pragma unroll
-  for (int j = 0; j < NCH; ++j) {
-    const int cc = threadIdx.x + j * kThreads;
-    if (cc < a.nch) {
-      float4* dst = reinterpret_cast<float4*>(a.part + (size_t)c * a.d + 8 * (size_t)cc);
-      __stcg(dst, make_float4(yacc[j][0], yacc[j][1], yacc[j][2], yacc[j][3]));
-      __stcg(dst + 1, make_float4(yacc[j][4], yacc[j][5], yacc[j][6], yacc[j][7]));
+  ffn_ring<DT, GATED, NCH>(a, xs, lst, lb, m, mh, nh, slots, full, empty, red,
+                           red + 2 * kGroup * 2 * kWarps, yacc, &s_bad);
+  __syncthreads();
+  // speculative copies of own hot neurons that turned out inactive must land
+  // before the block may exit
+  if (MODE == kFused && tid == kThreads && mh < nh_c) {
+    for (int j = 0; j < nh_c; ++j) {
+      bool used = false;
+      for (int k = 0; k < mh; ++k) used |= (lst[k] == c + j * P);
+      if (!used && !mbar_wait(full + j, 0u, a.limit_ns)) set_status(a.status, PI_ERR_TIMEOUT);
     }
   }
-  if (!grid_sync(a.bar, (unsigned)P, a.status, a.limit_ns)) return;
-  final_reduce(a, reinterpret_cast<float4*>(red));
+  if (compute) {
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      const int cc = tid + j * kThreads;
+      if (cc < a.nch) {
+        float4* dst = reinterpret_cast<float4*>(a.part + (size_t)c * a.d + 8 * (size_t)cc);
+        __stcg(dst, make_float4(yacc[j][0], yacc[j][1], yacc[j][2], yacc[j][3]));
+        __stcg(dst + 1, make_float4(yacc[j][4], yacc[j][5], yacc[j][6], yacc[j][7]));
+      }
+    }
+  }
+  const unsigned long long nb = (MODE == kFused) ? 2ull : 1ull;
+  if (!grid_sync(a.bar, s_base + nb * P, a.status, a.limit_ns)) return;
+  if (!compute) return;
+  final_reduce(a);
+  if (MODE == kFused) {
+    if (a.cnt_out && c == 0 && warp == 0) {
+      int sum = 0;
+      for (int b = lane; b < P; b += 32) sum += __ldcg(a.loc_tot + b);
+      sum = __reduce_add_sync(0xffffffffu, sum);
+      if (lane == 0) a.cnt_out[0] = sum;
+    }
+    if (a.idx_out) write_active_list(a, reinterpret_cast<int*>(red));
+  }
+}
+
+// ------------------------------------------------------------ offline packing
+// packed[i] = [W1 row(s) of i | W2 row of i], 16 bytes per thread-step.
+__global__ void pack_kernel(const uint4* W1, const uint4* W2, uint4* packed, int n, int d8,
+                            int m1) {
+  const long long rec = (long long)(m1 + 1) * d8;
+  const long long total = (long long)n * rec;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+       e += (long long)gridDim.x * blockDim.x) {
+    const long long i = e / rec, k = e - i * rec;
+    packed[e] = (k < (long long)m1 * d8) ? W1[i * m1 * d8 + k] : W2[i * d8 + (k - (long long)m1 * d8)];
+  }
 }
 
 // ------------------------------------------------------------ standalone predictor
@@ -501,7 +725,7 @@ template <int DT, int TB>
 __global__ void __launch_bounds__(256) predict_logits_kernel(const uint16_t* A, const float* b1,
                                                              const float* u, int n, int r,
                                                              int batch, float* logits) {
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem[];
   float* us = reinterpret_cast<float*>(smem);  // [batch][r]
   for (int e = threadIdx.x; e < batch * r; e += 256) us[e] = u[e];
   __syncthreads();
@@ -617,8 +841,12 @@ __global__ void __launch_bounds__(1024) union_kernel(const float* logits, int n,
 
 // Failure-path diagnostic: one grid-wide wait whose last arrival never
 // comes (expected = grid + 1), so every block gives up after limit_ns.
-__global__ void wait_timeout_kernel(GridBar bar, int* status, unsigned long long limit_ns) {
-  grid_sync(bar, gridDim.x + 1u, status, limit_ns);
+__global__ void wait_timeout_kernel(unsigned long long* bar, int* status,
+                                    unsigned long long limit_ns) {
+  __shared__ unsigned long long s_base;
+  if (threadIdx.x == 0) s_base = grid_base(bar, gridDim.x);
+  __syncthreads();
+  grid_sync(bar, s_base + gridDim.x + 1u, status, limit_ns);
 }
 
 }  // namespace pik

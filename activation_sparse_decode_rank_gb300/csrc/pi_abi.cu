@@ -21,7 +21,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // Byte offsets of the workspace regions.
 struct WsLayout {
-  size_t ctrl, upart, loc_cnt, loc_idx, part, u, logits, total;
+  size_t ctrl, upart, loc_tot, mask, part, u, logits, total;
 };
 
 WsLayout ws_layout(const pi_ffn_desc& D, int batch) {
@@ -32,10 +32,10 @@ WsLayout ws_layout(const pi_ffn_desc& D, int batch) {
     off += round_up(bytes > 0 ? bytes : 1, kAlign);
     return o;
   };
-  L.ctrl = take(256);  // barrier counter (+0) and generation (+128)
+  L.ctrl = take(256);  // grid barrier arrival counter (64-bit)
   L.upart = take(sizeof(float) * (size_t)D.r * kSMax);
-  L.loc_cnt = take(sizeof(int) * kPMax);
-  L.loc_idx = take(sizeof(int) * (size_t)D.n);
+  L.loc_tot = take(sizeof(int) * kPMax);
+  L.mask = take((size_t)D.n);
   L.part = take(sizeof(float) * (size_t)kPMax * D.d);
   L.u = take(sizeof(float) * (size_t)batch * D.r);
   L.logits = take(sizeof(float) * (size_t)batch * D.n);
@@ -51,17 +51,19 @@ pi_status check_desc(const pi_ffn_desc* D) {
   if (D->n < 1 || D->n > (1 << 24)) return PI_ERR_SHAPE;
   if (D->gated != 0 && D->gated != 1) return PI_ERR_SHAPE;
   if (D->hot_prefix < 0 || D->hot_prefix > D->n) return PI_ERR_SHAPE;
+  if (D->layout != PI_LAYOUT_SPLIT && D->layout != PI_LAYOUT_PACKED) return PI_ERR_SHAPE;
   return PI_OK;
 }
 
 pi_status check_weights(const pi_ffn_desc& D, const pi_layer_weights* w, bool need_pred) {
   if (!w) return PI_ERR_NULL;
-  if (!w->b1 || !w->W1 || !w->W2) return PI_ERR_NULL;
+  if (!w->b1 || !w->W1) return PI_ERR_NULL;
+  if (D.layout == PI_LAYOUT_SPLIT && !w->W2) return PI_ERR_NULL;
+  if (D.layout == PI_LAYOUT_PACKED && w->W2) return PI_ERR_SHAPE;
   if (need_pred && (!w->A || !w->Bm)) return PI_ERR_NULL;
   const void* ps[] = {w->A, w->Bm, w->b1, w->W1, w->W2, w->b2};
   for (const void* p : ps)
     if (p && !aligned16(p)) return PI_ERR_ALIGN;
-  (void)D;
   return PI_OK;
 }
 
@@ -126,16 +128,43 @@ using FfnFn = void (*)(const FfnArgs);
 template <int MODE>
 FfnFn pick_ffn(int dtype, int gated, bool wide) {
   if (dtype == PI_F16) {
-    if (!gated) return wide ? ffn_kernel<0, false, 2, 4, MODE> : ffn_kernel<0, false, 1, 8, MODE>;
-    return wide ? ffn_kernel<0, true, 2, 2, MODE> : ffn_kernel<0, true, 1, 4, MODE>;
+    if (!gated) return wide ? ffn_kernel<0, false, 2, MODE> : ffn_kernel<0, false, 1, MODE>;
+    return wide ? ffn_kernel<0, true, 2, MODE> : ffn_kernel<0, true, 1, MODE>;
   }
-  if (!gated) return wide ? ffn_kernel<1, false, 2, 4, MODE> : ffn_kernel<1, false, 1, 8, MODE>;
-  return wide ? ffn_kernel<1, true, 2, 2, MODE> : ffn_kernel<1, true, 1, 4, MODE>;
+  if (!gated) return wide ? ffn_kernel<1, false, 2, MODE> : ffn_kernel<1, false, 1, MODE>;
+  return wide ? ffn_kernel<1, true, 2, MODE> : ffn_kernel<1, true, 1, MODE>;
 }
 
-// Fills the shape fields, grid size and shared-memory layout of a
-// persistent launch; returns the dynamic shared-memory bytes (0 = error).
-int plan_ffn(const pi_ffn_desc& D, int mode, int P, int positions, FfnArgs& a) {
+// Shared-memory layout of a persistent launch for a given predictor-row
+// placement; returns the bytes before the ring slots (16-byte aligned).
+int layout_fixed(const pi_ffn_desc& D, int mode, int P, int rows_max, int a_in_smem, FfnArgs& a) {
+  int off = 0;
+  auto take = [&](int bytes, int align) {
+    off = (off + align - 1) / align * align;
+    const int o = off;
+    off += bytes;
+    return o;
+  };
+  a.o_xs = take(4 * D.d, 16);
+  a.o_lst = take(4 * (rows_max + kMaxSlots), 16);
+  a.o_lb = take(4 * (rows_max + kMaxSlots), 16);
+  a.o_red = take(4 * (2 * kGroup * 2 * kWarps + 2 * kGroup + 64), 16);  // butterfly partials, h
+  a.o_mbar = take(2 * 8 * kMaxSlots, 16);
+  a.o_us = a.o_As = a.o_b1s = a.o_flag = a.o_off = 0;
+  (void)P;
+  if (mode == kFused) {
+    a.o_us = take(4 * D.r, 16);
+    a.o_b1s = take(4 * rows_max, 16);
+    a.o_flag = take(rows_max, 16);
+    if (a_in_smem) a.o_As = take(rows_max * (2 * D.r + 16), 16);
+  }
+  return (off + 127) / 128 * 128;
+}
+
+// Fills the shape fields, grid size and shared-memory plan of a persistent
+// launch; returns the dynamic shared-memory bytes, or 0 if the shape does
+// not fit.
+int plan_ffn(const pi_ffn_desc& D, int mode, int P, int positions, int smem_limit, FfnArgs& a) {
   a.d = D.d;
   a.n = D.n;
   a.r = D.r;
@@ -146,25 +175,43 @@ int plan_ffn(const pi_ffn_desc& D, int mode, int P, int positions, FfnArgs& a) {
   int S = 1;
   while (D.r * S < P && S < kSMax && (D.d / (2 * S)) % 8 == 0 && D.d / (2 * S) >= 256) S *= 2;
   a.S = S;
-  int off = 0;
-  auto take = [&](int bytes) {
-    const int o = off;
-    off += (bytes + 15) & ~15;
-    return o;
+  a.slot_bytes = (D.gated ? 3 : 2) * D.d * 2;
+  a.packed = D.layout == PI_LAYOUT_PACKED ? 1 : 0;
+  a.a_stride = 2 * D.r + 16;
+  auto slots_for = [&](int fixed) {
+    const int ns = (smem_limit - fixed) / a.slot_bytes;
+    return ns < kMaxSlots ? ns : kMaxSlots;
   };
-  a.o_xs = take(4 * D.d);
-  a.o_wl = take(4 * a.rows_max);
-  a.o_red = take(16 * kThreads);
-  a.o_us = a.o_As = a.o_b1s = a.o_flag = a.o_lst = a.o_off = 0;
+  a.a_in_smem = 0;
+  int fixed = layout_fixed(D, mode, P, a.rows_max, 0, a);
+  int ns = slots_for(fixed);
   if (mode == kFused) {
-    a.o_us = take(4 * D.r);
-    a.o_As = take(2 * a.rows_max * D.r);
-    a.o_b1s = take(4 * a.rows_max);
-    a.o_flag = take(4 * a.rows_max);
-    a.o_lst = take(4 * a.rows_max);
-    a.o_off = take(4 * (P + 1));
+    FfnArgs t = a;
+    const int fixed_s = layout_fixed(D, mode, P, a.rows_max, 1, t);
+    const int ns_s = slots_for(fixed_s);
+    if (ns_s >= 10 || ns_s >= ns) {  // stage A only if the ring stays deep
+      a = t;
+      a.a_in_smem = 1;
+      fixed = fixed_s;
+      ns = ns_s;
+    } else {
+      layout_fixed(D, mode, P, a.rows_max, 0, a);
+    }
   }
-  return off;
+  if (ns < 2) return 0;
+  a.ns = ns;
+  a.nh = 0;
+  if (mode == kFused && D.hot_prefix > 0) {
+    const int hot_per_block = (D.hot_prefix + P - 1) / P;
+    const int cap = ns - 2 * kGroup > ns / 4 ? ns - 2 * kGroup : ns / 4;  // keep two rounds of cold slots
+    a.nh = hot_per_block < cap ? hot_per_block : cap;
+    if (a.nh < 0) a.nh = 0;
+  }
+  if (a.ns - a.nh < kGroup) a.nh = a.ns - kGroup;  // the ring must hold one round
+  if (a.nh < 0) return 0;
+  a.grp = kGroup;
+  a.o_slots = fixed;
+  return fixed + ns * a.slot_bytes;
 }
 
 template <int MODE>
@@ -172,17 +219,18 @@ pi_status launch_ffn(const pi_ffn_desc& D, FfnArgs& a, int positions, cudaStream
   DevInfo di;
   pi_status s = dev_info(&di);
   if (s != PI_OK) return s;
-  const int P = di.sms < kPMax ? di.sms : kPMax;
+  const int P = di.sms < kPMax ? di.sms : kPMax;  // also <= kThreads (one scan lane per block)
   const bool wide = (D.d / 8) > kThreads;
   FfnFn fn = pick_ffn<MODE>(D.dtype, D.gated, wide);
-  const int smem = plan_ffn(D, MODE, P, positions, a);
-  if (smem + 1024 > di.smem_optin) return PI_ERR_SHAPE;
+  const int limit = di.smem_optin - 1024;  // static shared memory and margin
+  const int smem = plan_ffn(D, MODE, P, positions, limit, a);
+  if (smem == 0 || a.grp < 1) return PI_ERR_SHAPE;
   s = ensure_smem(reinterpret_cast<const void*>(fn), smem);
   if (s != PI_OK) return s;
   a.limit_ns = wait_limit_ns();
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)P);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kBlock);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -195,11 +243,10 @@ pi_status launch_ffn(const pi_ffn_desc& D, FfnArgs& a, int positions, cudaStream
 
 void bind_ws(FfnArgs& a, const WsLayout& L, void* ws) {
   char* b = static_cast<char*>(ws);
-  a.bar.count = reinterpret_cast<unsigned*>(b + L.ctrl);
-  a.bar.gen = reinterpret_cast<unsigned*>(b + L.ctrl + 128);
+  a.bar = reinterpret_cast<unsigned long long*>(b + L.ctrl);
   a.upart = reinterpret_cast<float*>(b + L.upart);
-  a.loc_cnt = reinterpret_cast<int*>(b + L.loc_cnt);
-  a.loc_idx = reinterpret_cast<int*>(b + L.loc_idx);
+  a.loc_tot = reinterpret_cast<int*>(b + L.loc_tot);
+  a.mask = reinterpret_cast<unsigned char*>(b + L.mask);
   a.part = reinterpret_cast<float*>(b + L.part);
 }
 
@@ -392,10 +439,29 @@ pi_status pi_layer_decode(const pi_ffn_desc* desc, const pi_layer_weights* w, co
     a.y = y + t * d;
     a.idx_out = idx_out ? idx_out + t * n : nullptr;
     a.cnt_out = cnt_out ? cnt_out + t : nullptr;
+    if (!a.idx_out) a.mask = nullptr;  // the mask is only kept to build idx_out
     a.status = dev_status;
     s = launch_ffn<kFused>(*desc, a, desc->n, reinterpret_cast<cudaStream_t>(stream));
     if (s != PI_OK) return s;
   }
+  return PI_OK;
+}
+
+pi_status pi_pack_weights(const pi_ffn_desc* desc, const void* W1, const void* W2, void* packed,
+                          pi_stream stream) {
+  pi_ffn_desc D = desc ? *desc : pi_ffn_desc{};
+  D.layout = PI_LAYOUT_SPLIT;
+  pi_status s = check_desc(desc ? &D : nullptr);
+  if (s != PI_OK) return s;
+  if (!W1 || !W2 || !packed) return PI_ERR_NULL;
+  if (!aligned16(W1) || !aligned16(W2) || !aligned16(packed)) return PI_ERR_ALIGN;
+  const int m1 = D.gated ? 2 : 1, d8 = D.d / 8;
+  const long long total = (long long)D.n * (m1 + 1) * d8;
+  const unsigned grid = (unsigned)((total + 255) / 256 < 65535 * 8 ? (total + 255) / 256 : 65535 * 8);
+  pack_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(W1), static_cast<const uint4*>(W2), static_cast<uint4*>(packed), D.n,
+      d8, m1);
+  if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
   return PI_OK;
 }
 
@@ -405,11 +471,8 @@ pi_status pi_selftest_wait_timeout(int32_t* dev_status, void* ws, size_t ws_byte
   if (!aligned16(dev_status) || !aligned16(ws)) return PI_ERR_ALIGN;
   if (ws_bytes < 256) return PI_ERR_WORKSPACE;
   if (limit_ns < 1000 || limit_ns > 5000000000LL) return PI_ERR_SHAPE;
-  GridBar bar;
-  bar.count = static_cast<unsigned*>(ws);
-  bar.gen = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + 128);
   wait_timeout_kernel<<<4, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      bar, dev_status, (unsigned long long)limit_ns);
+      static_cast<unsigned long long*>(ws), dev_status, (unsigned long long)limit_ns);
   if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
   return PI_OK;
 }

@@ -243,10 +243,15 @@ def run_ours(args):
     pred_bytes = n * r * 2 + r * d * 2 + n * 4
     step_bytes_est = pred_bytes + w["density"] * n * m_rows * d * 2
     R = args.replicas if args.replicas > 0 else max(2, math.ceil(3 * l2 / step_bytes_est))
+    desc = pi.make_desc(d, n, r, w["dtype"], gated, hot, packed=args.layout == "packed")
     base = [up(L.A), up(L.Bm), up(L.b1), up(L.W1), up(L.W2), up(L.b2)]
-    reps = [base] + [[t.clone() for t in base] for _ in range(R - 1)]
-    layer_bytes = sum(t.numel() * t.element_size() for t in base)
-    desc = pi.make_desc(d, n, r, w["dtype"], gated, hot)
+    if args.layout == "packed":
+        # offline step: one record per neuron ([W1 row(s) | W2 row])
+        rec = torch.empty((n, m_rows * d), dtype=torch.int16, device=dev)
+        pi.check(pi.pi_pack_weights(desc, base[3], base[4], rec), "pi_pack_weights")
+        base = [base[0], base[1], base[2], rec, None, base[5]]
+    reps = [base] + [[t.clone() if t is not None else None for t in base] for _ in range(R - 1)]
+    layer_bytes = sum(t.numel() * t.element_size() for t in base if t is not None)
     wts = [pi.make_weights(*rp) for rp in reps]
 
     G = min(args.steps, args.graph_len)
@@ -424,7 +429,7 @@ def run_ours(args):
         "data": "synthetic",
         "config": {
             "workload": args.workload, "batch": 1, "weights": w["dtype"], "density": w["density"],
-            "d": d, "n": n, "r": r, "gated": gated, "hot_prefix": hot,
+            "d": d, "n": n, "r": r, "gated": gated, "hot_prefix": hot, "layout": args.layout,
             "l2": (f"inputs larger than L2: {R} rotating weight replicas "
                    f"({R * layer_bytes / 1e9:.1f} GB; each step reads its own copy)"),
             "graph_len": G, "parallelism": "replicas" if world > 1 else "single GPU",
@@ -464,6 +469,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--replicas", type=int, default=0)
+    ap.add_argument("--layout", default="packed", choices=["packed", "split"])
     ap.add_argument("--hot", type=int, default=-1, help="hot-prefix length (-1: p_i >= 0.5)")
     ap.add_argument("--graph-len", type=int, default=2000)
     ap.add_argument("--e2e-steps", type=int, default=20000)

@@ -28,6 +28,7 @@
  *      W1  [n][d]      up projection, or gated [n][2][d]: per neuron the
  *                      gate row followed by the up row        (dtype)
  *      W2  [n][d]      down projection, one row per neuron   (dtype)
+ *      (or both in one per-neuron record: see pi_layout)
  *      b2  [d]         fp32 output bias, may be NULL (= 0)
  *      x   [batch][d]  fp32 activations;  y [batch][d] fp32 outputs
  *  - Alignment: every pointer passed must be 16-byte aligned.
@@ -79,6 +80,15 @@ typedef enum {
 
 typedef enum { PI_F16 = 0, PI_BF16 = 1 } pi_dtype;
 
+/* Storage of the FFN weights.
+ *  PI_LAYOUT_SPLIT : W1 [n][d] (gated [n][2][d]) and W2 [n][d], two matrices.
+ *  PI_LAYOUT_PACKED: one record per neuron, W1 [n][m d] with m = 2 (plain:
+ *                    up row, down row) or m = 3 (gated: gate, up, down rows);
+ *                    W2 must be NULL.  The same bytes, so the same results;
+ *                    a neuron's rows then arrive in one bulk copy.  Build it
+ *                    with pi_pack_weights.                                   */
+typedef enum { PI_LAYOUT_SPLIT = 0, PI_LAYOUT_PACKED = 1 } pi_layout;
+
 /* Shape of one FFN layer. */
 typedef struct {
   int32_t d;           /* model (hidden) dimension                              */
@@ -89,6 +99,7 @@ typedef struct {
   int32_t hot_prefix;  /* neurons [0, hot_prefix) form the hot block: their
                           rows are fetched towards the chip before the mask is
                           known (0 = off).  Never changes results.             */
+  int32_t layout;      /* pi_layout of W1 / W2                                  */
 } pi_ffn_desc;
 
 /* Device pointers of one layer's weights (layouts above). */
@@ -96,8 +107,8 @@ typedef struct {
   const void* A;
   const void* Bm;
   const float* b1;
-  const void* W1;
-  const void* W2;
+  const void* W1;  /* PI_LAYOUT_PACKED: the per-neuron records */
+  const void* W2;  /* PI_LAYOUT_PACKED: NULL                   */
   const float* b2; /* may be NULL */
 } pi_layer_weights;
 
@@ -178,6 +189,15 @@ pi_status pi_layer_decode(const pi_ffn_desc* desc, const pi_layer_weights* w,
                           const float* residual, int32_t* idx_out,
                           int32_t* cnt_out, int32_t* dev_status, void* ws,
                           size_t ws_bytes, pi_stream stream);
+
+/* Offline step: builds the PI_LAYOUT_PACKED records of a layer from its
+ * split matrices (desc->layout is ignored).  W1 [n][d] (gated [n][2][d]) and
+ * W2 [n][d] are read, packed [n][m d] is written (m = 2, or 3 if gated); the
+ * buffers must not overlap.  Like the neuron reordering it accompanies
+ * ("Offline Section": neurons are laid out by their profiled activation
+ * before serving), it runs once per layer, not per token. */
+pi_status pi_pack_weights(const pi_ffn_desc* desc, const void* W1, const void* W2,
+                          void* packed, pi_stream stream);
 
 /* Static text of a status code. */
 const char* pi_status_string(pi_status s);

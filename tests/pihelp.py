@@ -32,9 +32,10 @@ def up(a, dev):
 
 
 class DevLayer:
-    """A generated layer resident on the GPU, with its descriptor."""
+    """A generated layer resident on the GPU, with its descriptor.  packed:
+    the weights are held as per-neuron records built by pi_pack_weights."""
 
-    def __init__(self, L, dev, hot_prefix: int = 0, with_b2: bool = True):
+    def __init__(self, L, dev, hot_prefix: int = 0, with_b2: bool = True, packed: bool = False):
         self.L = L
         self.dev = dev
         self.A = up(L.A, dev)
@@ -45,6 +46,22 @@ class DevLayer:
         self.b2 = up(L.b2, dev) if (with_b2 and L.b2 is not None) else None
         self.desc = pi.make_desc(L.d, L.n, L.r, L.dtype, L.gated, hot_prefix)
         self.w = pi.make_weights(self.A, self.Bm, self.b1, self.W1, self.W2, self.b2)
+        self.packed = None
+        if packed:
+            self.set_packed(True)
+
+    def set_packed(self, on: bool):
+        """Switches the descriptor and weights between the two layouts."""
+        if on and self.packed is None:
+            m = 3 if self.L.gated else 2
+            self.packed = torch.empty((self.L.n, m * self.L.d), dtype=torch.int16, device=self.dev)
+            pi.check(pi.pi_pack_weights(self.desc, self.W1, self.W2, self.packed),
+                     "pi_pack_weights")
+        self.desc.layout = pi.PI_LAYOUT_PACKED if on else pi.PI_LAYOUT_SPLIT
+        if on:
+            self.w = pi.make_weights(self.A, self.Bm, self.b1, self.packed, None, self.b2)
+        else:
+            self.w = pi.make_weights(self.A, self.Bm, self.b1, self.W1, self.W2, self.b2)
 
     def workspace(self, batch=1):
         return pi.workspace(self.desc, batch, self.dev)

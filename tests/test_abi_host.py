@@ -62,6 +62,9 @@ def test_workspace_size_host_only(lib):
     assert pi.pi_workspace_size(bad, 1) == 0
     bad = pi.make_desc(4096, 16384, 128, hot_prefix=16385)
     assert pi.pi_workspace_size(bad, 1) == 0
+    bad = pi.make_desc(4096, 16384, 128)
+    bad.layout = 2
+    assert pi.pi_workspace_size(bad, 1) == 0
     assert pi.pi_workspace_size(d, 0) == 0 and pi.pi_workspace_size(d, 33) == 0
 
 
@@ -100,6 +103,15 @@ def test_host_validation_before_launch(lib):
                         None) == pi.PI_ERR_NULL   # capacity may overflow: dev_status needed
     assert L.pi_compact(P, 100, 2, P, P, 100, P, None, P, P, None, 0,
                         None) == pi.PI_ERR_NULL   # union without its count
+    # packed layout: W2 must be NULL; split layout: W2 required
+    dp = pi.make_desc(1024, 4096, 64, "f16", packed=True)
+    assert L.pi_layer_decode(by(dp), by(w), P, 1, P, None, None, None, P, P, ws_bytes,
+                             None) == pi.PI_ERR_SHAPE
+    w3 = pi.make_weights(P, P, P, P, None, None)
+    assert L.pi_layer_decode(by(d), by(w3), P, 1, P, None, None, None, P, P, ws_bytes,
+                             None) == pi.PI_ERR_NULL
+    assert L.pi_pack_weights(by(d), P, None, P, None) == pi.PI_ERR_NULL
+    assert L.pi_pack_weights(by(d), P + 2, P, P, None) == pi.PI_ERR_ALIGN
     assert L.pi_selftest_wait_timeout(P, P, 64, 1000000, None) == pi.PI_ERR_WORKSPACE
     assert L.pi_selftest_wait_timeout(P, P, 4096, 10, None) == pi.PI_ERR_SHAPE
 

@@ -323,6 +323,51 @@ def test_layer_decode_in_cuda_graph():
     torch.testing.assert_close(y, ref, rtol=0, atol=0)
 
 
+# ---------------------------------------------------------------- packed layout
+@pytest.mark.parametrize("name", ["ragged_d200_n1001_r24", "ragged_gated_d136_n777_r16",
+                                  "opt6.7b_d4096_n16384", "llama2_7b_gated_d4096_n11008"])
+def test_pack_weights_bit_exact(name):
+    D = layer(name)
+    L = D.L
+    D.set_packed(True)
+    try:
+        got = D.packed.cpu().numpy().view(np.uint16)
+        m1 = 2 if L.gated else 1
+        want = np.concatenate([L.W1.reshape(L.n, m1 * L.d), L.W2], axis=1)
+        np.testing.assert_array_equal(got, want)
+    finally:
+        D.set_packed(False)
+
+
+@pytest.mark.parametrize("name", list(WL))
+def test_packed_layout_same_results(name):
+    """The packed records hold the same bytes: every entry point gives
+    bit-identical outputs on both layouts."""
+    D = layer(name)
+    L = D.L
+    x = synth.gen_x(40, 0, 1, L.d)
+    a = _decode(D, x)
+    _, lo = oracle.predict(L, x)
+    idx = oracle.compact(lo[0])
+    ys, _ = _sparse(D, x, idx)
+    D.set_packed(True)
+    try:
+        b = _decode(D, x)
+        yp, st = _sparse(D, x, idx)
+        assert b["status"] == 0 and st == 0
+        np.testing.assert_array_equal(a["y"], b["y"])
+        np.testing.assert_array_equal(a["idx"][0], b["idx"][0])
+        np.testing.assert_array_equal(ys, yp)
+        if L.d <= 4096:
+            y = torch.empty((1, L.d), device=DEV)
+            pi.check(pi.pi_dense_ffn(D.desc, D.w, up(x, DEV), 1, y, D.workspace()))
+            torch.cuda.synchronize()
+            yd = oracle.dense_ffn(L, x[0])
+            assert float(np.abs(y[0].cpu().numpy() - yd).max()) / float(np.abs(yd).max()) <= Y_TOL
+    finally:
+        D.set_packed(False)
+
+
 # ---------------------------------------------------------------- failure path
 def test_bounded_wait_times_out_and_reports():
     D = layer("tiny_d1024_n4096")
