@@ -83,6 +83,7 @@ SIGNATURES = {
     "pi_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "pi_selftest_wait_timeout": (ctypes.c_int, [_P, _P, _SZ, _I64, _P]),
     "pi_pack_weights": (ctypes.c_int, [_DESC, _P, _P, _P, _P]),
+    "pi_layer_decode_static": (ctypes.c_int, [_DESC, _W, _P, _P, _P, _P, _P, _P, _P]),
 }
 
 
@@ -194,6 +195,18 @@ def pi_layer_decode(desc, w, x, batch, y, residual, idx_out, cnt_out, dev_status
 def pi_pack_weights(desc, W1, W2, packed, stream=None) -> int:
     return lib().pi_pack_weights(ctypes.byref(desc), _ptr(W1), _ptr(W2), _ptr(packed),
                                  _stream(stream))
+
+
+def pi_layer_decode_static(desc, w, x, y, residual, idx_out, cnt_out, dev_status,
+                           stream=None) -> int:
+    """pi_layer_decode for one token with the library's fixed scratch instead
+    of a workspace (for callers that cannot allocate device memory)."""
+    return lib().pi_layer_decode_static(ctypes.byref(desc), ctypes.byref(w), _ptr(x), _ptr(y),
+                                        _ptr(residual), _ptr(idx_out), _ptr(cnt_out),
+                                        _ptr(dev_status), _stream(stream))
+
+
+PI_STATIC_SCRATCH_BYTES = 8 << 20
 
 
 def pi_status_string(status: int) -> str:

@@ -259,9 +259,89 @@ void bind_weights(FfnArgs& a, const pi_layer_weights& w) {
   a.b2 = w.b2;
 }
 
+// ------------------------------------------------------------ fixed scratch
+// Scratch of pi_layer_decode_static: a fixed array in the device image
+// instead of a caller workspace.  Zero at load; every call clears its
+// barrier block before launching.
+static __device__ __align__(256) unsigned char g_static_scratch[PI_STATIC_SCRATCH_BYTES];
+
+std::unordered_map<int, void*> g_static_ptr;  // device -> address of g_static_scratch
+
+// Device address of g_static_scratch on the current device, looked up once
+// per device (host code only has a stand-in for the symbol).
+pi_status static_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PI_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_static_ptr.find(dev);
+  if (it == g_static_ptr.end()) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) return PI_ERR_CUDA;
+    it = g_static_ptr.emplace(dev, p).first;
+  }
+  *out = it->second;
+  return PI_OK;
+}
+
+// Regions of the fused batch-1 kernel's scratch with exactly P partial rows.
+WsLayout static_layout(const pi_ffn_desc& D, int P) {
+  WsLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += round_up(bytes > 0 ? bytes : 1, kAlign);
+    return o;
+  };
+  L.ctrl = take(256);
+  L.upart = take(sizeof(float) * (size_t)D.r * kSMax);
+  L.loc_tot = take(sizeof(int) * (size_t)P);
+  L.mask = take((size_t)D.n);
+  L.part = take(sizeof(float) * (size_t)P * D.d);
+  L.u = L.logits = 0;
+  L.total = off;
+  return L;
+}
+
 }  // namespace
 
 extern "C" {
+
+pi_status pi_layer_decode_static(const pi_ffn_desc* desc, const pi_layer_weights* w, const float* x,
+                                 float* y, const float* residual, int32_t* idx_out,
+                                 int32_t* cnt_out, int32_t* dev_status, pi_stream stream) {
+  pi_status s = check_desc(desc);
+  if (s != PI_OK) return s;
+  s = check_weights(*desc, w, true);
+  if (s != PI_OK) return s;
+  if (!x || !y || !dev_status) return PI_ERR_NULL;
+  const void* ps[] = {x, y, residual, idx_out, cnt_out, dev_status};
+  for (const void* p : ps)
+    if (p && !aligned16(p)) return PI_ERR_ALIGN;
+  DevInfo di;
+  s = dev_info(&di);
+  if (s != PI_OK) return s;
+  const int P = di.sms < kPMax ? di.sms : kPMax;
+  const WsLayout L = static_layout(*desc, P);
+  if (L.total > PI_STATIC_SCRATCH_BYTES) return PI_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  s = static_scratch(&scratch);
+  if (s != PI_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(static_cast<char*>(scratch) + L.ctrl, 0, 256, st) != cudaSuccess)
+    return PI_ERR_CUDA;
+  FfnArgs a{};
+  bind_weights(a, *w);
+  bind_ws(a, L, scratch);
+  a.x = x;
+  a.residual = residual;
+  a.y = y;
+  a.idx_out = idx_out;
+  a.cnt_out = cnt_out;
+  a.status = dev_status;
+  if (!a.idx_out) a.mask = nullptr;
+  return launch_ffn<kFused>(*desc, a, desc->n, st);
+}
+
 
 size_t pi_workspace_size(const pi_ffn_desc* desc, int32_t batch) {
   if (check_desc(desc) != PI_OK) return 0;

@@ -190,6 +190,30 @@ pi_status pi_layer_decode(const pi_ffn_desc* desc, const pi_layer_weights* w,
                           int32_t* cnt_out, int32_t* dev_status, void* ws,
                           size_t ws_bytes, pi_stream stream);
 
+/* pi_layer_decode for batch 1 without a caller-provided workspace.  The
+ * paper has no counterpart to this call; it exists for callers that cannot
+ * allocate device memory: for example a plugin inside a host framework that
+ * owns all device memory and hands plugins no allocator, or a latency-bound
+ * loop that must not call cudaMalloc (it can synchronise the device).
+ * Inputs and outputs are the caller's, as in pi_layer_decode with batch = 1
+ * and ws = NULL.  The scratch is a fixed array of PI_STATIC_SCRATCH_BYTES in
+ * the library's device image, held by every GPU that loads the library until
+ * the process exits.  Shapes whose scratch does not fit (about P * d * 4
+ * bytes of partial sums plus n bytes, P = the GPU's SM count) are rejected
+ * with PI_ERR_WORKSPACE before anything is launched.  The call allocates and
+ * frees nothing; each call clears the array's barrier block with one
+ * cudaMemsetAsync on `stream` before its launch.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress, with that
+ * device current); make that first call before any stream capture.  All
+ * calls share the one array: calls that overlap on the GPU (other streams,
+ * other threads) race and corrupt each other's results; issue them in one
+ * stream order. */
+#define PI_STATIC_SCRATCH_BYTES (8u << 20)
+pi_status pi_layer_decode_static(const pi_ffn_desc* desc, const pi_layer_weights* w,
+                                 const float* x, float* y, const float* residual,
+                                 int32_t* idx_out, int32_t* cnt_out, int32_t* dev_status,
+                                 pi_stream stream);
+
 /* Offline step: builds the PI_LAYOUT_PACKED records of a layer from its
  * split matrices (desc->layout is ignored).  W1 [n][d] (gated [n][2][d]) and
  * W2 [n][d] are read, packed [n][m d] is written (m = 2, or 3 if gated); the
