@@ -19,6 +19,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "synth.c")
 _HDR = os.path.join(_HERE, "synth.h")
 _LIB = os.path.join(_HERE, "libsynth.so")
+_GPU_SRC = os.path.join(_HERE, "synth_gpu.cu")
+_GPU_LIB = os.path.join(_HERE, "libsynth_gpu.so")
+_gpu_lib = None
 _lock = threading.Lock()
 _lib = None
 
@@ -37,6 +40,30 @@ def build(force: bool = False) -> str:
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB)
     return _LIB
+
+
+def build_gpu(force: bool = False) -> str:
+    """Compile libsynth_gpu.so (the generator's CUDA build) next to the sources."""
+    stale = (not os.path.exists(_GPU_LIB)) or os.path.getmtime(_GPU_SRC) > os.path.getmtime(_GPU_LIB)
+    if force or stale:
+        tmp = _GPU_LIB + f".tmp{os.getpid()}"
+        cmd = ["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17",
+               "-Xcompiler", "-fPIC", "-shared", "-o", tmp, _GPU_SRC]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _GPU_LIB)
+    return _GPU_LIB
+
+
+def gpu_lib():
+    global _gpu_lib
+    with _lock:
+        if _gpu_lib is None:
+            L = ctypes.CDLL(build_gpu())
+            L.sy_gpu_gen_layer.restype = ctypes.c_int
+            L.sy_gpu_gen_layer.argtypes = [ctypes.c_int] * 6 + [ctypes.c_uint64, ctypes.c_double] + \
+                [ctypes.c_void_p] * 7
+            _gpu_lib = L
+    return _gpu_lib
 
 
 class _Spec(ctypes.Structure):
@@ -212,3 +239,45 @@ def permute_layer(layer: Layer, perm: np.ndarray) -> Layer:
                  np.ascontiguousarray(layer.W1[perm]),
                  np.ascontiguousarray(layer.W2[perm]), layer.b2,
                  dict(layer.meta, permuted=True))
+
+
+def make_layer_gpu(d: int, n: int, r: int, dtype: str = "f16", gated: bool = False,
+                   alpha: float = 0.9, density: float | None = 0.06,
+                   zipf_c: float | None = None, seed: int = 0, layer: int = 0,
+                   bias_scale: float = 1.0, noise: float = 0.05, p_cap: float = 0.9,
+                   device="cuda", stream=None) -> dict:
+    """The same layer as make_layer, generated on the GPU into torch tensors
+    (16-bit patterns as int16; b1 / b2 fp32).  For layers too large to build
+    quickly on the host."""
+    import torch
+    if zipf_c is None:
+        zipf_c = zipf_calibrate(n, alpha, density, p_cap)
+    p = zipf_probs(n, alpha, zipf_c, p_cap)
+    b1 = np.array([bias_scale * probit(v) for v in p], dtype=np.float32)
+    dev = torch.device(device)
+    A = torch.empty((n, r), dtype=torch.int16, device=dev)
+    Bm = torch.empty((r, d), dtype=torch.int16, device=dev)
+    W1 = torch.empty((n, 2, d) if gated else (n, d), dtype=torch.int16, device=dev)
+    W2 = torch.empty((n, d), dtype=torch.int16, device=dev)
+    A64 = torch.empty(n * r, dtype=torch.float64, device=dev)
+    B64 = torch.empty(r * d, dtype=torch.float64, device=dev)
+    st = torch.cuda.current_stream(dev).cuda_stream if stream is None else stream.cuda_stream
+    rc = gpu_lib().sy_gpu_gen_layer(d, n, r, DTYPES[dtype], int(gated), layer, seed, noise,
+                                    A.data_ptr(), Bm.data_ptr(), W1.data_ptr(), W2.data_ptr(),
+                                    A64.data_ptr(), B64.data_ptr(), st)
+    if rc != 0:
+        raise RuntimeError(f"sy_gpu_gen_layer failed: cuda error {rc}")
+    del A64, B64
+    return dict(d=d, n=n, r=r, dtype=dtype, gated=bool(gated), A=A, Bm=Bm,
+                b1=torch.from_numpy(b1).to(dev), W1=W1, W2=W2,
+                b2=torch.zeros(d, dtype=torch.float32, device=dev),
+                meta=dict(alpha=alpha, zipf_c=zipf_c, p_cap=p_cap, bias_scale=bias_scale,
+                          noise=noise, seed=seed, layer=layer))
+
+
+def to_host_layer(g: dict) -> Layer:
+    """Host copy (uint16 patterns) of a GPU-generated layer, for the oracle."""
+    cpu = lambda t: t.cpu().numpy()
+    return Layer(g["d"], g["n"], g["r"], g["dtype"], g["gated"], cpu(g["A"]).view(np.uint16),
+                 cpu(g["Bm"]).view(np.uint16), cpu(g["b1"]), cpu(g["W1"]).view(np.uint16),
+                 cpu(g["W2"]).view(np.uint16), cpu(g["b2"]), dict(g["meta"]))
