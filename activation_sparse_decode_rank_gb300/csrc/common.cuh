@@ -129,6 +129,14 @@ __device__ __forceinline__ void mbar_init(uint64_t* m, unsigned count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(m)), "r"(count) : "memory");
 }
 
+// Programmatic dependent launch: wait until the preceding kernel in the
+// stream has completed and its memory is visible (returns at once if the
+// launch has no programmatic dependency), and let the next kernel launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Barrier among the kThreads compute threads only (the producer warp keeps
 // running its own loop).
 __device__ __forceinline__ void compute_sync() {

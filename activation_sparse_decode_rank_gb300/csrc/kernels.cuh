@@ -29,7 +29,7 @@ struct FfnArgs {
   int a_stride;    // bytes between staged predictor rows (2 r + 16: conflict-free reads)
   int ns;          // ring slots (one neuron's W1 row(s) + W2 row each)
   int nh;          // fused: slots [0, nh) take the block's own hot neurons up front
-  int grp;         // (unused: rounds hold kGroup neurons; needs ns - nh >= kGroup)
+  int grp;         // neurons per round: 1, 2 or kGroup, <= ns - nh
   int slot_bytes;
   int packed;      // PI_LAYOUT_PACKED: W1 holds [n][m d] per-neuron records
   // dynamic shared-memory offsets (bytes)
@@ -175,10 +175,11 @@ __device__ void own_logits(const FfnArgs& a, const unsigned char* As, const floa
 //   B. eight lanes of warp 0 add the kWarps partials in order, add the bias
 //      and apply ReLU (times the up projection, gated);
 //   C. each thread adds h_q times its chunks of the round's W2 rows.
-// Every sum has a fixed order, so results are deterministic.  Needs kGroup
-// <= ns - nh (no round waits for a slot that only its own release would
-// free).  lb[k] is b1 of neuron lst[k]; red holds 2 x kGroup x NV x kWarps
-// floats, hbuf 2 x kGroup.
+// Every sum has a fixed order, so results are deterministic.  A round holds
+// a.grp <= kGroup neurons; a.grp <= ns - nh (no round waits for a slot that
+// only its own release would free), and a shallow ring takes smaller rounds
+// so that copies stay in flight while a round is computed.  lb[k] is b1 of
+// neuron lst[k]; red holds 2 x kGroup x NV x kWarps floats, hbuf 2 x kGroup.
 template <int DT, bool GATED, int NCH>
 __device__ void ffn_ring(const FfnArgs& a, const float* xs, const int* lst, const float* lb, int m,
                          int mh, int nh, unsigned char* slots, uint64_t* full, uint64_t* empty,
@@ -216,8 +217,9 @@ __device__ void ffn_ring(const FfnArgs& a, const float* xs, const int* lst, cons
   }
   int cslot = 0, cpar = 0;  // ring position of the next cold entry
   int buf = 0;
-  for (int g0 = 0; g0 < m; g0 += kGroup) {
-    const int kg = min(kGroup, m - g0);
+  const int grp = a.grp;
+  for (int g0 = 0; g0 < m; g0 += grp) {
+    const int kg = min(grp, m - g0);
     int sl[kGroup];
 #pragma unroll
     for (int q = 0; q < kGroup; ++q) {
@@ -419,16 +421,18 @@ __global__ void __launch_bounds__(kBlock, 1) ffn_kernel(const FfnArgs a) {
   const int hot_own = (MODE == kFused && c < a.hot) ? (a.hot - 1 - c) / P + 1 : 0;
   const int nh = (MODE == kFused) ? a.nh : 0;
   const int nh_c = min(nh, hot_own);  // own hot neurons whose rows go to slots up front
+  // Everything before pdl_wait() reads only weights: with programmatic
+  // dependent launch it overlaps the end of the previous step, whose
+  // outputs (x, the workspace) are not touched until after the wait.
   if (tid == 0) {
     for (int s = 0; s < a.ns; ++s) {
       mbar_init(full + s, 1u);
       mbar_init(empty + s, (unsigned)kWarps);
     }
     fence_mbar_init();
-    // weights that do not depend on x go out first: own hot neurons' rows
+    // own hot neurons' rows go out first
     for (int j = 0; j < nh_c; ++j) issue_neuron<GATED>(a, slots, full, j, c + j * P);
     s_bad = 0;
-    s_base = grid_base(a.bar, (unsigned)P);
   }
   int m = 0, mh = 0;
 
@@ -438,20 +442,11 @@ __global__ void __launch_bounds__(kBlock, 1) ffn_kernel(const FfnArgs a) {
     float* b1s = reinterpret_cast<float*>(smem + a.o_b1s);
     float* us = reinterpret_cast<float*>(smem + a.o_us);
     unsigned char* flag = smem + a.o_flag;
-    int* off = reinterpret_cast<int*>(smem + a.o_off);
     const int units = a.r * a.S;
     const int seg = a.d / a.S;
     const int segc = seg >> 3;
 
-    // 1. x first: it is the latency-critical input
-    float4 xv4[4];
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const int i = tid + h * kThreads;
-      xv4[h] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (compute && i < (a.d >> 2)) xv4[h] = __ldg(reinterpret_cast<const float4*>(a.x) + i);
-    }
-    // 2. this block's first predictor-stage-1 units (Bm chunks)
+    // 1. this block's first predictor-stage-1 units (Bm chunks)
     uint4 bw[2][2];
 #pragma unroll
     for (int uu = 0; uu < 2; ++uu) {
@@ -482,12 +477,12 @@ __global__ void __launch_bounds__(kBlock, 1) ffn_kernel(const FfnArgs a) {
       }
       for (int j = tid; j < rows; j += kThreads) cp_async4(b1s + j, a.b1 + c + (size_t)j * P);
       cp_async_commit();
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const int i = tid + h * kThreads;
-        if (i < (a.d >> 2)) reinterpret_cast<float4*>(xs)[i] = xv4[h];
-      }
     }
+    // 2. the previous step's outputs: x and the barrier state
+    pdl_wait();
+    if (tid == 0) s_base = grid_base(a.bar, (unsigned)P);
+    for (int i = tid; i < (a.d >> 2); i += kBlock)
+      reinterpret_cast<float4*>(xs)[i] = __ldg(reinterpret_cast<const float4*>(a.x) + i);
     __syncthreads();
     // 4. predictor stage 1: partial dot products of the units
     for (int q0 = c; q0 < units; q0 += 2 * P) {
@@ -582,6 +577,8 @@ __global__ void __launch_bounds__(kBlock, 1) ffn_kernel(const FfnArgs a) {
     m = s_m;
     mh = s_mh;
   } else {
+    pdl_wait();
+    if (tid == 0) s_base = grid_base(a.bar, (unsigned)P);
     for (int i = tid; i < (a.d >> 2); i += kBlock)
       reinterpret_cast<float4*>(xs)[i] = __ldg(reinterpret_cast<const float4*>(a.x) + i);
     int total;
@@ -655,6 +652,7 @@ __global__ void __launch_bounds__(kBlock, 1) ffn_kernel(const FfnArgs a) {
   }
   const unsigned long long nb = (MODE == kFused) ? 2ull : 1ull;
   if (!grid_sync(a.bar, s_base + nb * P, a.status, a.limit_ns)) return;
+  pdl_trigger();  // no grid-wide wait is left: the next step may start launching
   if (!compute) return;
   final_reduce(a);
   if (MODE == kFused) {

@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <mutex>
+#include <string>
 #include <unordered_map>
 
 #include "kernels.cuh"
@@ -76,6 +77,7 @@ std::mutex g_mu;
 std::unordered_map<int, DevInfo> g_dev;
 std::unordered_map<const void*, int> g_smem_set;  // kernel -> dynamic smem attribute set (per process)
 unsigned long long g_limit_ns = 0;
+int g_launch_mode = -1;  // 0: cooperative launch, 1: programmatic dependent launch
 
 pi_status dev_info(DevInfo* out) {
   int dev = 0;
@@ -104,6 +106,21 @@ unsigned long long wait_limit_ns() {
     }
   }
   return g_limit_ns;
+}
+
+// How persistent grids are launched.  Default: programmatic dependent
+// launch, which lets a step's weight prefetch overlap the end of the
+// previous step in the same stream; every block is resident because the grid
+// has one block per SM and a block fills an SM.  PI_LAUNCH=cooperative
+// selects a cooperative launch instead (the driver then also checks
+// co-residency, but consecutive steps do not overlap).
+int launch_mode() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_launch_mode < 0) {
+    const char* e = std::getenv("PI_LAUNCH");
+    g_launch_mode = (e && std::string(e) == "cooperative") ? 0 : 1;
+  }
+  return g_launch_mode;
 }
 
 pi_status ensure_smem(const void* fn, int bytes) {
@@ -207,9 +224,11 @@ int plan_ffn(const pi_ffn_desc& D, int mode, int P, int positions, int smem_limi
     a.nh = hot_per_block < cap ? hot_per_block : cap;
     if (a.nh < 0) a.nh = 0;
   }
-  if (a.ns - a.nh < kGroup) a.nh = a.ns - kGroup;  // the ring must hold one round
-  if (a.nh < 0) return 0;
-  a.grp = kGroup;
+  if (a.ns < 8) a.nh = 0;  // shallow ring: keep every slot for the active rows
+  // rounds of kGroup neurons need two rounds of cold slots to keep copies in
+  // flight; a shallower ring takes rounds of 2 (or 1)
+  const int nc = a.ns - a.nh;
+  a.grp = nc >= 2 * kGroup ? kGroup : (nc >= 4 ? 2 : 1);
   a.o_slots = fixed;
   return fixed + ns * a.slot_bytes;
 }
@@ -234,8 +253,18 @@ pi_status launch_ffn(const pi_ffn_desc& D, FfnArgs& a, int positions, cudaStream
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  if (launch_mode() == 0) {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  } else {
+    int per_sm = 0;  // the grid must fit at one block per SM
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kBlock, (size_t)smem) !=
+        cudaSuccess)
+      return PI_ERR_CUDA;
+    if (per_sm < 1) return PI_ERR_LAUNCH;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+  }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return map_launch_error(cudaLaunchKernelEx(&cfg, fn, a));
