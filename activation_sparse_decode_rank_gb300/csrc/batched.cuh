@@ -1,0 +1,406 @@
+// batched.cuh — batched decode (2 <= batch <= 32) of the activation-sparse
+// FFN on tensor cores.
+//
+// Every token keeps its own predicted mask; the union of the tokens' active
+// neurons is read once and turned into a dense tile contraction:
+//   phase 1  H[u][t] = mask_t(u) ? act(W1[U_u] . x_t + b1[U_u]) : 0
+//            (act = ReLU, or ReLU(gate) * up), one tile of 64 union neurons
+//            at a time, A = activations (tokens x d), B = W1 rows;
+//   phase 2  Y_g[t][cols] = sum_{u in group g} H[u][t] W2[U_u][cols]
+//            over 8 neuron groups x (P / 8) column slices;
+//   phase 3  y[t] = b2 + sum_g Y_g[t] (g ascending) (+ residual).
+// Tensor-core operands are 16-bit: x and H are split into a high and a low
+// 16-bit part (x = hi + lo), so each product is taken twice and the sum keeps
+// about 16 more bits than one rounding would.  mma.sync m16n8k16 with fp32
+// accumulation; operands staged in shared memory by cp.async, fragments by
+// ldmatrix (rows padded by 16 bytes: conflict-free).
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace pik {
+
+constexpr int kBT = 64;          // union neurons per phase-1 tile
+constexpr int kBK = 128;         // columns per phase-1 chunk
+constexpr int kBStages = 3;      // cp.async pipeline depth
+constexpr int kBN2 = 32;         // union neurons per phase-2 chunk
+constexpr int kGroups2 = 8;      // neuron groups of phase 2
+
+struct BatchArgs {
+  int d, n, batch, bp;        // bp: batch padded to 16 or 32 (rows of the A operand)
+  int P;                      // phase-1 grid; phase-2 grid = kGroups2 * slices
+  int slices, cw;             // phase-2 column slices and their width (multiple of 8)
+  int packed;                 // PI_LAYOUT_PACKED
+  int rec;                    // elements per packed record ((gated ? 3 : 2) d)
+  const uint16_t* W1;
+  const uint16_t* W2;
+  const float* b1;
+  const float* b2;
+  const float* x;             // [batch][d]
+  const float* residual;      // [batch][d] or NULL
+  float* y;                   // [batch][d]
+  const int* uidx;            // union neurons, ascending
+  const int* ucnt;            // union count (device)
+  const uint32_t* tmask;      // token bitmask per union position
+  uint16_t* xhi;              // [bp][d] activations, high and low 16-bit parts
+  uint16_t* xlo;
+  uint16_t* hhi;              // [bp][hs] H transposed (token-major), high / low parts
+  uint16_t* hlo;
+  int hs;                     // row stride of hhi / hlo (>= n + kBN2, multiple of 8)
+  float* part;                // [kGroups2][bp][d]
+  int* status;
+};
+
+// ---------------------------------------------------------------- helpers
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t (&r)[2], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(smem_u32(p)));
+}
+
+// D += A (16x16, row) * B (16x8, col), 16-bit inputs, fp32 accumulate.
+template <int DT>
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  if (DT == 0)
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+  else
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// v = hi + lo with hi, lo 16-bit (lo = the rounding error of hi).
+template <int DT>
+__device__ __forceinline__ void split16(float v, uint16_t* hi, uint16_t* lo) {
+  if (DT == 0) {
+    const __half h = __float2half_rn(v);
+    const __half l = __float2half_rn(v - __half2float(h));
+    *hi = __half_as_ushort(h);
+    *lo = __half_as_ushort(l);
+  } else {
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    const __nv_bfloat16 l = __float2bfloat16_rn(v - __bfloat162float(h));
+    *hi = __bfloat16_as_ushort(h);
+    *lo = __bfloat16_as_ushort(l);
+  }
+}
+
+// ---------------------------------------------------------------- phase 0
+// xhi/xlo[t][j] = split(x[t][j]) for t < batch, 0 for padded rows.
+template <int DT>
+__global__ void bsplit_x_kernel(const BatchArgs a) {
+  const long long tot = (long long)a.bp * a.d;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < tot;
+       e += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(e / a.d);
+    uint16_t hi = 0, lo = 0;
+    if (t < a.batch) split16<DT>(a.x[e], &hi, &lo);
+    a.xhi[e] = hi;
+    a.xlo[e] = lo;
+  }
+}
+
+// ---------------------------------------------------------------- phase 1
+// Shared-memory layout of one pipeline stage: W1 rows [kBT][kBK] (gated:
+// gate rows then up rows), then x high / low parts [bp][kBK]; rows padded by
+// 16 bytes.
+constexpr int kRowB = kBK * 2 + 16;  // bytes per staged row
+
+template <bool GATED>
+__host__ __device__ constexpr int bup_stage_bytes(int bp) {
+  return ((GATED ? 2 : 1) * kBT + 2 * bp) * kRowB;
+}
+
+template <int DT, bool GATED, int MT>
+__global__ void __launch_bounds__(512, 1) bup_kernel(const BatchArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int U = __ldg(a.ucnt);
+  const int lo_u = (int)((long long)blockIdx.x * U / a.P);
+  const int hi_u = (int)((long long)(blockIdx.x + 1) * U / a.P);
+  const int stage_bytes = bup_stage_bytes<GATED>(a.bp);
+  constexpr int NW = GATED ? 2 : 1;
+  // warp -> (m tile, n tile, k parity): MT = 2: 16 fragments, one per warp;
+  // MT = 1: 8 fragments, two warps each, taking alternate k-steps.
+  const int nt = warp & 7;
+  const int mt = (MT == 2) ? (warp >> 3) : 0;
+  const int kpar = (MT == 2) ? 0 : (warp >> 3);
+  const int ksteps = kBK / 16;
+  const int nchunks = a.d / kBK;
+  float* comb = reinterpret_cast<float*>(smem + kBStages * stage_bytes);  // [8][32][4 * NW]
+  const size_t w1s = a.packed ? (size_t)a.rec : (GATED ? 2 * (size_t)a.d : (size_t)a.d);
+
+  for (int t0 = lo_u; t0 < hi_u; t0 += kBT) {
+    const int tn = min(kBT, hi_u - t0);
+    // issue the cp.async loads of chunk ch into stage ch % kBStages
+    auto issue = [&](int ch) {
+      unsigned char* st = smem + (ch % kBStages) * stage_bytes;
+      const int k0 = ch * kBK;
+      constexpr int CPR = kBK / 8;  // 16-byte pieces per row
+      for (int e = tid; e < NW * kBT * CPR; e += 512) {
+        const int rw = e / CPR, pc = e - rw * CPR;
+        const int w = rw / kBT, row = rw - w * kBT;
+        unsigned char* dst = st + (size_t)rw * kRowB + 16 * pc;
+        if (row < tn) {
+          const int nid = __ldg(a.uidx + t0 + row);
+          cp_async16(dst, a.W1 + (size_t)nid * w1s + (size_t)w * a.d + k0 + 8 * pc);
+        } else {
+          *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      unsigned char* xs_ = st + (size_t)NW * kBT * kRowB;
+      for (int e = tid; e < 2 * a.bp * CPR; e += 512) {
+        const int rw = e / CPR, pc = e - rw * CPR;
+        const int part = rw / a.bp, t = rw - part * a.bp;
+        const uint16_t* src = (part == 0 ? a.xhi : a.xlo) + (size_t)t * a.d + k0 + 8 * pc;
+        cp_async16(xs_ + (size_t)rw * kRowB + 16 * pc, src);
+      }
+    };
+    float acc[NW][4];
+#pragma unroll
+    for (int w = 0; w < NW; ++w)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[w][e] = 0.f;
+    for (int ch = 0; ch < kBStages - 1; ++ch) {  // always kBStages - 1 groups
+      if (ch < nchunks) issue(ch);
+      cp_async_commit();
+    }
+    for (int ch = 0; ch < nchunks; ++ch) {
+      if (ch + kBStages - 1 < nchunks) issue(ch + kBStages - 1);
+      cp_async_commit();
+      asm volatile("cp.async.wait_group %0;" ::"n"(kBStages - 1) : "memory");
+      __syncthreads();
+      const unsigned char* st = smem + (ch % kBStages) * stage_bytes;
+      const unsigned char* xs_ = st + (size_t)NW * kBT * kRowB;
+      for (int ks = kpar; ks < ksteps; ks += (MT == 2 ? 1 : 2)) {
+        uint32_t ah[4], al[4];
+        {
+          // A fragment rows: tokens mt*16 .. +15, columns ks*16 .. +15
+          const int r = mt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+          const int cbyte = (ks * 16 + 8 * (lane >> 4)) * 2;
+          ldsm_x4(ah, xs_ + (size_t)r * kRowB + cbyte);
+          ldsm_x4(al, xs_ + (size_t)(a.bp + r) * kRowB + cbyte);
+        }
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          uint32_t b[2];
+          // B fragment: neurons nt*8 .. +7 (rows), k = ks*16 .. +15
+          const int r = w * kBT + nt * 8 + (lane & 7);
+          const int cbyte = (ks * 16 + 8 * ((lane >> 3) & 1)) * 2;
+          ldsm_x2(b, st + (size_t)r * kRowB + cbyte);
+          mma16816<DT>(acc[w], ah, b);
+          mma16816<DT>(acc[w], al, b);
+        }
+      }
+      __syncthreads();
+    }
+    // MT = 1: the two k-parity halves meet (fixed order: even + odd)
+    if (MT == 1) {
+      if (kpar == 1) {
+#pragma unroll
+        for (int w = 0; w < NW; ++w)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) comb[(nt * 32 + lane) * 4 * NW + w * 4 + e] = acc[w][e];
+      }
+      __syncthreads();
+      if (kpar == 0) {
+#pragma unroll
+        for (int w = 0; w < NW; ++w)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[w][e] += comb[(nt * 32 + lane) * 4 * NW + w * 4 + e];
+      }
+    }
+    // epilogue: bias, activation, the token's own mask bit, split, store H^T
+    if (MT == 2 || kpar == 0) {
+      const int g = lane >> 2, tq = lane & 3;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int t = mt * 16 + g + 8 * (e >> 1);      // token (row of the fragment)
+        const int col = nt * 8 + 2 * tq + (e & 1);     // neuron within the tile
+        if (col < tn && t < a.batch) {
+          const int pos = t0 + col;
+          const int nid = __ldg(a.uidx + pos);
+          float h = acc[0][e] + __ldg(a.b1 + nid);
+          h = h > 0.f ? h : 0.f;  // ReLU; ReLU(0) = 0
+          if (GATED) h *= acc[NW - 1][e];
+          if (!((__ldg(a.tmask + pos) >> t) & 1u)) h = 0.f;  // token t skips this neuron
+          uint16_t hh, hl;
+          split16<DT>(h, &hh, &hl);
+          a.hhi[(size_t)t * a.hs + pos] = hh;
+          a.hlo[(size_t)t * a.hs + pos] = hl;
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------- phase 2
+// Block (g, s): union positions of group g, columns [s cw, s cw + cw).
+// Stage: W2 rows [kBN2][cw] then H^T high / low [bp][kBN2], rows padded.
+__host__ __device__ inline int bdn_w2_row(int cw) { return cw * 2 + 16; }
+constexpr int kHRowB = kBN2 * 2 + 16;
+__host__ __device__ inline int bdn_stage_bytes(int cw, int bp) {
+  return kBN2 * bdn_w2_row(cw) + 2 * bp * kHRowB;
+}
+
+template <int DT, int MT>
+__global__ void __launch_bounds__(512, 1) bdown_kernel(const BatchArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = blockIdx.x / a.slices, s = blockIdx.x - g * a.slices;
+  const int U = __ldg(a.ucnt);
+  // group boundaries on multiples of 8 positions: every 16-byte piece of an
+  // H^T row starts 16-byte aligned; the last group ends at U
+  const int lo_u = (int)((long long)g * U / kGroups2) & ~7;
+  const int hi_u = (g == kGroups2 - 1) ? U : ((int)((long long)(g + 1) * U / kGroups2) & ~7);
+  const int c0 = s * a.cw;
+  const int cn = min(a.cw, a.d - c0);  // columns of this slice (multiple of 8)
+  if (cn <= 0) return;
+  const int NT = cn / 8;
+  const int w2row = bdn_w2_row(a.cw);
+  const int stage_bytes = bdn_stage_bytes(a.cw, a.bp);
+  const size_t w2s = a.packed ? (size_t)a.rec : (size_t)a.d;  // W2 rows (packed: inside records)
+  const uint16_t* w2base = a.W2;
+  // warp w owns n tiles w, w + 16, w + 32 (< NT), all m tiles
+  constexpr int NTW = 3;
+  float acc[NTW][MT][4];
+#pragma unroll
+  for (int q = 0; q < NTW; ++q)
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[q][m][e] = 0.f;
+  const int nchunks = (hi_u - lo_u + kBN2 - 1) / kBN2;
+  auto issue = [&](int ch) {
+    unsigned char* st = smem + (ch % kBStages) * stage_bytes;
+    const int p0 = lo_u + ch * kBN2;
+    const int cpr = cn / 8;  // 16-byte pieces per W2 row piece
+    for (int e = tid; e < kBN2 * cpr; e += 512) {
+      const int row = e / cpr, pc = e - row * cpr;
+      unsigned char* dst = st + (size_t)row * w2row + 16 * pc;
+      if (p0 + row < hi_u) {
+        const int nid = __ldg(a.uidx + p0 + row);
+        cp_async16(dst, w2base + (size_t)nid * w2s + c0 + 8 * pc);
+      } else {
+        *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    unsigned char* hs_ = st + (size_t)kBN2 * w2row;
+    constexpr int HPR = kBN2 / 8;
+    for (int e = tid; e < 2 * a.bp * HPR; e += 512) {
+      const int rw = e / HPR, pc = e - rw * HPR;
+      const int part = rw / a.bp, t = rw - part * a.bp;
+      unsigned char* dst = hs_ + (size_t)rw * kHRowB + 16 * pc;
+      const int q0 = p0 + 8 * pc;  // first position of the piece (multiple of 8)
+      const uint16_t* src = (part == 0 ? a.hhi : a.hlo) + (size_t)t * a.hs + q0;
+      if (q0 + 8 <= hi_u) {
+        cp_async16(dst, src);
+      } else if (q0 >= hi_u) {
+        // past the group: never written by phase 1 for this call
+        *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+      } else {
+        // the piece that holds the union end (last group only)
+        uint16_t v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = (q0 + i < hi_u) ? src[i] : (uint16_t)0;
+        uint4 pk;
+        pk.x = v[0] | ((uint32_t)v[1] << 16);
+        pk.y = v[2] | ((uint32_t)v[3] << 16);
+        pk.z = v[4] | ((uint32_t)v[5] << 16);
+        pk.w = v[6] | ((uint32_t)v[7] << 16);
+        *reinterpret_cast<uint4*>(dst) = pk;
+      }
+    }
+  };
+  for (int ch = 0; ch < kBStages - 1; ++ch) {  // always kBStages - 1 groups
+    if (ch < nchunks) issue(ch);
+    cp_async_commit();
+  }
+  for (int ch = 0; ch < nchunks; ++ch) {
+    if (ch + kBStages - 1 < nchunks) issue(ch + kBStages - 1);
+    cp_async_commit();
+    asm volatile("cp.async.wait_group %0;" ::"n"(kBStages - 1) : "memory");
+    __syncthreads();
+    const unsigned char* st = smem + (ch % kBStages) * stage_bytes;
+    const unsigned char* hs_ = st + (size_t)kBN2 * w2row;
+#pragma unroll
+    for (int ks = 0; ks < kBN2 / 16; ++ks) {
+      uint32_t ah[MT][4], al[MT][4];
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        const int r = m * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+        const int cbyte = (ks * 16 + 8 * (lane >> 4)) * 2;
+        ldsm_x4(ah[m], hs_ + (size_t)r * kHRowB + cbyte);
+        ldsm_x4(al[m], hs_ + (size_t)(a.bp + r) * kHRowB + cbyte);
+      }
+#pragma unroll
+      for (int q = 0; q < NTW; ++q) {
+        const int ntile = warp + 16 * q;
+        if (ntile < NT) {
+          uint32_t b[2];
+          // W2 stored [k = neuron][n = column]: transposed load gives the
+          // (k pair, n) layout of the B operand
+          const int kr = ks * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+          ldsm_x2_t(b, st + (size_t)kr * w2row + ntile * 16);
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            mma16816<DT>(acc[q][m], ah[m], b);
+            mma16816<DT>(acc[q][m], al[m], b);
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+  // partial Y of group g, this slice
+  const int gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+  for (int q = 0; q < NTW; ++q) {
+    const int ntile = warp + 16 * q;
+    if (ntile < NT) {
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = m * 16 + gq + 8 * (e >> 1);
+          const int col = c0 + ntile * 8 + 2 * tq + (e & 1);
+          a.part[((size_t)g * a.bp + t) * a.d + col] = acc[q][m][e];
+        }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- phase 3
+__global__ void bsum_kernel(const BatchArgs a) {
+  const long long tot = (long long)a.batch * a.d;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < tot;
+       e += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(e / a.d), j = (int)(e - (long long)t * a.d);
+    float s = 0.f;
+    for (int g = 0; g < kGroups2; ++g) s += a.part[((size_t)g * a.bp + t) * a.d + j];
+    if (a.b2) s += a.b2[j];
+    if (a.residual) s += a.residual[e];
+    a.y[e] = s;
+  }
+}
+
+}  // namespace pik

@@ -9,6 +9,7 @@
 #include <unordered_map>
 
 #include "kernels.cuh"
+#include "batched.cuh"
 
 using namespace pik;
 
@@ -23,7 +24,13 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // Byte offsets of the workspace regions.
 struct WsLayout {
   size_t ctrl, upart, loc_tot, mask, part, u, logits, total;
+  // batched path (batch > 1)
+  size_t bidx, bcnt, uidx, ucnt, tmask, xhi, xlo, hhi, hlo, bpart;
+  int bp, hs;
 };
+
+int batch_pad(int batch) { return batch <= 16 ? 16 : 32; }
+int h_stride(int n) { return (int)round_up((size_t)n + kBN2, 64); }
 
 WsLayout ws_layout(const pi_ffn_desc& D, int batch) {
   WsLayout L{};
@@ -40,6 +47,20 @@ WsLayout ws_layout(const pi_ffn_desc& D, int batch) {
   L.part = take(sizeof(float) * (size_t)kPMax * D.d);
   L.u = take(sizeof(float) * (size_t)batch * D.r);
   L.logits = take(sizeof(float) * (size_t)batch * D.n);
+  L.bp = batch_pad(batch);
+  L.hs = h_stride(D.n);
+  if (batch > 1) {
+    L.bidx = take(sizeof(int) * (size_t)batch * D.n);
+    L.bcnt = take(sizeof(int) * (size_t)batch);
+    L.uidx = take(sizeof(int) * (size_t)D.n);
+    L.ucnt = take(sizeof(int));
+    L.tmask = take(sizeof(uint32_t) * (size_t)D.n);
+    L.xhi = take(2 * (size_t)L.bp * D.d);
+    L.xlo = take(2 * (size_t)L.bp * D.d);
+    L.hhi = take(2 * (size_t)L.bp * L.hs);
+    L.hlo = take(2 * (size_t)L.bp * L.hs);
+    L.bpart = take(sizeof(float) * (size_t)kGroups2 * L.bp * D.d);
+  }
   L.total = off;
   return L;
 }
@@ -288,6 +309,81 @@ void bind_weights(FfnArgs& a, const pi_layer_weights& w) {
   a.b2 = w.b2;
 }
 
+// ------------------------------------------------------------ batched path
+// The three tensor-core phases of a batched sparse FFN over the union of the
+// tokens' active neurons (uidx / ucnt / tmask in device memory).
+pi_status launch_batched(const pi_ffn_desc& D, const pi_layer_weights& w, const float* x,
+                         int batch, const int* uidx, const int* ucnt, const uint32_t* tmask,
+                         float* y, const float* residual, const WsLayout& L, void* ws,
+                         cudaStream_t st) {
+  DevInfo di;
+  pi_status s = dev_info(&di);
+  if (s != PI_OK) return s;
+  char* b = static_cast<char*>(ws);
+  BatchArgs a{};
+  a.d = D.d;
+  a.n = D.n;
+  a.batch = batch;
+  a.bp = L.bp;
+  a.P = di.sms;
+  a.slices = di.sms / kGroups2 > 0 ? di.sms / kGroups2 : 1;
+  a.cw = (int)round_up((size_t)((D.d + a.slices - 1) / a.slices), 8);
+  a.packed = D.layout == PI_LAYOUT_PACKED;
+  a.rec = (D.gated ? 3 : 2) * D.d;
+  a.W1 = static_cast<const uint16_t*>(w.W1);
+  a.W2 = a.packed ? a.W1 + (size_t)(D.gated ? 2 : 1) * D.d : static_cast<const uint16_t*>(w.W2);
+  a.b1 = w.b1;
+  a.b2 = w.b2;
+  a.x = x;
+  a.residual = residual;
+  a.y = y;
+  a.uidx = uidx;
+  a.ucnt = ucnt;
+  a.tmask = tmask;
+  a.xhi = reinterpret_cast<uint16_t*>(b + L.xhi);
+  a.xlo = reinterpret_cast<uint16_t*>(b + L.xlo);
+  a.hhi = reinterpret_cast<uint16_t*>(b + L.hhi);
+  a.hlo = reinterpret_cast<uint16_t*>(b + L.hlo);
+  a.hs = L.hs;
+  a.part = reinterpret_cast<float*>(b + L.bpart);
+  const bool bf = D.dtype == PI_BF16;
+  const bool m2 = a.bp == 32;
+  // phase 0: split x
+  if (bf) bsplit_x_kernel<1><<<di.sms * 4, 256, 0, st>>>(a);
+  else bsplit_x_kernel<0><<<di.sms * 4, 256, 0, st>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
+  // phase 1
+  const int nw = D.gated ? 2 : 1;
+  const int smem1 = kBStages * ((nw * kBT + 2 * a.bp) * kRowB) + 8 * 32 * 4 * nw * 4;
+  using Fn = void (*)(const BatchArgs);
+  Fn f1;
+  if (!bf) {
+    if (!D.gated) f1 = m2 ? bup_kernel<0, false, 2> : bup_kernel<0, false, 1>;
+    else f1 = m2 ? bup_kernel<0, true, 2> : bup_kernel<0, true, 1>;
+  } else {
+    if (!D.gated) f1 = m2 ? bup_kernel<1, false, 2> : bup_kernel<1, false, 1>;
+    else f1 = m2 ? bup_kernel<1, true, 2> : bup_kernel<1, true, 1>;
+  }
+  if (smem1 + 1024 > di.smem_optin) return PI_ERR_SHAPE;
+  s = ensure_smem(reinterpret_cast<const void*>(f1), smem1);
+  if (s != PI_OK) return s;
+  f1<<<a.P, 512, smem1, st>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
+  // phase 2
+  const int smem2 = kBStages * bdn_stage_bytes(a.cw, a.bp);
+  Fn f2 = bf ? (m2 ? bdown_kernel<1, 2> : bdown_kernel<1, 1>)
+             : (m2 ? bdown_kernel<0, 2> : bdown_kernel<0, 1>);
+  if (smem2 + 1024 > di.smem_optin || a.cw / 8 > 48) return PI_ERR_SHAPE;
+  s = ensure_smem(reinterpret_cast<const void*>(f2), smem2);
+  if (s != PI_OK) return s;
+  f2<<<kGroups2 * a.slices, 512, smem2, st>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
+  // phase 3
+  bsum_kernel<<<di.sms * 4, 256, 0, st>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
+  return PI_OK;
+}
+
 // ------------------------------------------------------------ fixed scratch
 // Scratch of pi_layer_decode_static: a fixed array in the device image
 // instead of a caller workspace.  Zero at load; every call clears its
@@ -466,14 +562,26 @@ pi_status pi_sparse_ffn(const pi_ffn_desc* desc, const pi_layer_weights* w, cons
                         const int32_t* union_idx, const int32_t* union_cnt,
                         const uint32_t* tok_mask, float* y, int32_t* dev_status, void* ws,
                         size_t ws_bytes, pi_stream stream) {
-  (void)union_idx;
-  (void)union_cnt;
-  (void)tok_mask;
   pi_status s = check_desc(desc);
   if (s != PI_OK) return s;
-  if (batch != 1) return PI_ERR_SHAPE;
+  if (batch < 1 || batch > kMaxBatch) return PI_ERR_SHAPE;
   s = check_weights(*desc, w, false);
   if (s != PI_OK) return s;
+  if (batch > 1) {
+    if (!x || !y || !union_idx || !union_cnt || !tok_mask || !ws) return PI_ERR_NULL;
+    const void* pb[] = {x, y, union_idx, union_cnt, tok_mask, ws};
+    for (const void* p : pb)
+      if (!aligned16(p)) return PI_ERR_ALIGN;
+    if (desc->d % kBK) return PI_ERR_SHAPE;  // the batched path tiles d by 128
+    const WsLayout L = ws_layout(*desc, batch);
+    if (ws_bytes < L.total) return PI_ERR_WORKSPACE;
+    (void)idx;
+    (void)cnt;
+    (void)cap;
+    (void)dev_status;
+    return launch_batched(*desc, *w, x, batch, union_idx, union_cnt, tok_mask, y, nullptr, L, ws,
+                          reinterpret_cast<cudaStream_t>(stream));
+  }
   if (!x || !y || !idx || !cnt || !dev_status || !ws) return PI_ERR_NULL;
   const void* ps[] = {x, y, idx, cnt, dev_status, ws};
   for (const void* p : ps)
@@ -539,6 +647,24 @@ pi_status pi_layer_decode(const pi_ffn_desc* desc, const pi_layer_weights* w, co
   const WsLayout L = ws_layout(*desc, batch);
   if (ws_bytes < L.total) return PI_ERR_WORKSPACE;
   const size_t d = (size_t)desc->d, n = (size_t)desc->n;
+  if (batch > 1 && desc->d % kBK == 0) {
+    // batched: predictor over all tokens (A, Bm read once), per-token lists,
+    // their union, then the tensor-core contraction over the union
+    char* b = static_cast<char*>(ws);
+    float* logits = reinterpret_cast<float*>(b + L.logits);
+    int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(b + L.bidx);
+    int32_t* cnt = cnt_out ? cnt_out : reinterpret_cast<int32_t*>(b + L.bcnt);
+    int32_t* uidx = reinterpret_cast<int32_t*>(b + L.uidx);
+    int32_t* ucnt = reinterpret_cast<int32_t*>(b + L.ucnt);
+    uint32_t* tmask = reinterpret_cast<uint32_t*>(b + L.tmask);
+    s = pi_predict(desc, w->A, w->Bm, w->b1, x, batch, logits, ws, ws_bytes, stream);
+    if (s != PI_OK) return s;
+    s = pi_compact(logits, desc->n, batch, idx, cnt, desc->n, uidx, ucnt, tmask, dev_status, ws,
+                   ws_bytes, stream);
+    if (s != PI_OK) return s;
+    return launch_batched(*desc, *w, x, batch, uidx, ucnt, tmask, y, residual, L, ws,
+                          reinterpret_cast<cudaStream_t>(stream));
+  }
   for (int t = 0; t < batch; ++t) {
     FfnArgs a{};
     bind_weights(a, *w);

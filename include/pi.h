@@ -158,7 +158,10 @@ pi_status pi_compact(const float* logits, int32_t n, int32_t batch,
  * written to *dev_status.
  * batch > 1: the union form; union_idx / union_cnt / tok_mask as written by
  * pi_compact, and token t uses exactly the union neurons whose mask bit t is
- * set, so y[t] equals the batch-1 result for token t. */
+ * set, so y[t] equals the batch-1 result for token t (idx, cnt, cap and
+ * dev_status are then unused).  The union's rows are read once and
+ * contracted with all tokens on the tensor cores (16-bit operands with a
+ * high/low split of x and h, fp32 accumulation); needs d % 128 == 0. */
 pi_status pi_sparse_ffn(const pi_ffn_desc* desc, const pi_layer_weights* w,
                         const float* x, int32_t batch, const int32_t* idx,
                         const int32_t* cnt, int32_t cap,
@@ -177,8 +180,9 @@ pi_status pi_dense_ffn(const pi_ffn_desc* desc, const pi_layer_weights* w,
 /* One decode step of one layer: predictor, compaction and sparse FFN
  * ("Online Section" end to end).  batch == 1 runs as one persistent launch
  * whose grid-wide waits are bounded (PI_ERR_TIMEOUT on *dev_status if one
- * runs out).  batch > 1 runs the batched predictor, the union compaction
- * and the batched sparse FFN.
+ * runs out).  batch > 1 (with d % 128 == 0) runs the batched predictor,
+ * the per-token compaction and their union, and the batched sparse FFN on
+ * the tensor cores; otherwise one batch-1 step per token.
  *     y[t] = (residual ? residual[t] : 0) + FFN_sparse(x[t])
  * residual may be NULL; pass residual = x for a residual stack.  idx_out
  * ([batch][n]) and cnt_out ([batch]) may be NULL; when given they receive

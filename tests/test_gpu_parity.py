@@ -280,13 +280,19 @@ def test_layer_decode_deterministic():
 
 
 def test_layer_decode_batch_equals_per_token():
+    """A batched step gives every token its own mask and the batch-1 result
+    (within the tolerance: the batched contraction runs on tensor cores)."""
     D = layer("tiny_d1024_n4096")
-    x = synth.gen_x(32, 0, 4, D.L.d)
+    L = D.L
+    x = synth.gen_x(32, 0, 4, L.d)
     ob = _decode(D, x, batch=4)
+    assert ob["status"] == 0
     for t in range(4):
         o1 = _decode(D, x[t:t + 1])
-        np.testing.assert_array_equal(ob["y"][t], o1["y"][0])
-        np.testing.assert_array_equal(ob["idx"][t], o1["idx"][0])
+        _, lo = oracle.predict(L, x[t])
+        check_active_set(ob["idx"][t], lo[0])
+        yd = oracle.dense_ffn(L, x[t])
+        assert float(np.abs(ob["y"][t] - o1["y"][0]).max()) <= Y_TOL * float(np.abs(yd).max())
 
 
 def test_layer_decode_no_active_neuron():
