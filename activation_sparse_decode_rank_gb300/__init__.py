@@ -23,7 +23,7 @@ _lock = threading.Lock()
 _lib = None
 
 PI_OK, PI_ERR_NULL, PI_ERR_SHAPE, PI_ERR_DTYPE, PI_ERR_ALIGN, PI_ERR_WORKSPACE, \
-    PI_ERR_CAPACITY, PI_ERR_LAUNCH, PI_ERR_TIMEOUT, PI_ERR_CUDA, PI_ERR_INDEX = range(11)
+    PI_ERR_CAPACITY, PI_ERR_LAUNCH, PI_ERR_TIMEOUT, PI_ERR_CUDA, PI_ERR_INDEX, PI_ERR_RANGE = range(12)
 PI_F16, PI_BF16 = 0, 1
 PI_LAYOUT_SPLIT, PI_LAYOUT_PACKED = 0, 1
 
@@ -84,6 +84,8 @@ SIGNATURES = {
     "pi_selftest_wait_timeout": (ctypes.c_int, [_P, _P, _SZ, _I64, _P]),
     "pi_pack_weights": (ctypes.c_int, [_DESC, _P, _P, _P, _P]),
     "pi_layer_decode_static": (ctypes.c_int, [_DESC, _W, _P, _P, _P, _P, _P, _P, _P]),
+    "pi_decode_layers": (ctypes.c_int, [_P, _P, _I32, _I32, _P, _I32, _P, _P, _P, _P, _P, _SZ,
+                                        _P]),
 }
 
 
@@ -190,6 +192,21 @@ def pi_layer_decode(desc, w, x, batch, y, residual, idx_out, cnt_out, dev_status
                                  _ptr(residual), _ptr(idx_out), _ptr(cnt_out), _ptr(dev_status),
                                  _ptr(ws), ws.numel() if ws_bytes is None else ws_bytes,
                                  _stream(stream))
+
+
+def pi_decode_layers(descs, layers, J, x, chain, y, cnt_out, mask_out, dev_status, ws,
+                     ws_bytes=None, stream=None) -> int:
+    """descs / layers: lists of R descriptors and weight sets (step j uses
+    layer j % R)."""
+    R = len(layers)
+    if len(descs) != R:
+        raise ValueError("one descriptor per layer")
+    da = (pi_ffn_desc * R)(*descs)
+    wa = (pi_layer_weights * R)(*layers)
+    return lib().pi_decode_layers(ctypes.cast(da, ctypes.c_void_p), ctypes.cast(wa, ctypes.c_void_p),
+                                  R, J, _ptr(x), chain, _ptr(y), _ptr(cnt_out), _ptr(mask_out),
+                                  _ptr(dev_status), _ptr(ws),
+                                  ws.numel() if ws_bytes is None else ws_bytes, _stream(stream))
 
 
 def pi_pack_weights(desc, W1, W2, packed, stream=None) -> int:

@@ -43,6 +43,7 @@ struct BatchArgs {
   float* y;                   // [batch][d]
   const int* uidx;            // union neurons, ascending
   const int* ucnt;            // union count (device)
+  int dense;                  // 1: all n neurons, every token (uidx / ucnt / tmask unused)
   const uint32_t* tmask;      // token bitmask per union position
   uint16_t* xhi;              // [bp][d] activations, high and low 16-bit parts
   uint16_t* xlo;
@@ -133,7 +134,7 @@ template <int DT, bool GATED, int MT>
 __global__ void __launch_bounds__(512, 1) bup_kernel(const BatchArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int U = __ldg(a.ucnt);
+  const int U = a.dense ? a.n : __ldg(a.ucnt);
   const int lo_u = (int)((long long)blockIdx.x * U / a.P);
   const int hi_u = (int)((long long)(blockIdx.x + 1) * U / a.P);
   const int stage_bytes = bup_stage_bytes<GATED>(a.bp);
@@ -160,7 +161,7 @@ __global__ void __launch_bounds__(512, 1) bup_kernel(const BatchArgs a) {
         const int w = rw / kBT, row = rw - w * kBT;
         unsigned char* dst = st + (size_t)rw * kRowB + 16 * pc;
         if (row < tn) {
-          const int nid = __ldg(a.uidx + t0 + row);
+          const int nid = a.dense ? t0 + row : __ldg(a.uidx + t0 + row);
           cp_async16(dst, a.W1 + (size_t)nid * w1s + (size_t)w * a.d + k0 + 8 * pc);
         } else {
           *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
@@ -237,11 +238,11 @@ __global__ void __launch_bounds__(512, 1) bup_kernel(const BatchArgs a) {
         const int col = nt * 8 + 2 * tq + (e & 1);     // neuron within the tile
         if (col < tn && t < a.batch) {
           const int pos = t0 + col;
-          const int nid = __ldg(a.uidx + pos);
+          const int nid = a.dense ? pos : __ldg(a.uidx + pos);
           float h = acc[0][e] + __ldg(a.b1 + nid);
           h = h > 0.f ? h : 0.f;  // ReLU; ReLU(0) = 0
           if (GATED) h *= acc[NW - 1][e];
-          if (!((__ldg(a.tmask + pos) >> t) & 1u)) h = 0.f;  // token t skips this neuron
+          if (!a.dense && !((__ldg(a.tmask + pos) >> t) & 1u)) h = 0.f;  // token t skips it
           uint16_t hh, hl;
           split16<DT>(h, &hh, &hl);
           a.hhi[(size_t)t * a.hs + pos] = hh;
@@ -267,7 +268,7 @@ __global__ void __launch_bounds__(512, 1) bdown_kernel(const BatchArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x / a.slices, s = blockIdx.x - g * a.slices;
-  const int U = __ldg(a.ucnt);
+  const int U = a.dense ? a.n : __ldg(a.ucnt);
   // group boundaries on multiples of 8 positions: every 16-byte piece of an
   // H^T row starts 16-byte aligned; the last group ends at U
   const int lo_u = (int)((long long)g * U / kGroups2) & ~7;
@@ -298,7 +299,7 @@ __global__ void __launch_bounds__(512, 1) bdown_kernel(const BatchArgs a) {
       const int row = e / cpr, pc = e - row * cpr;
       unsigned char* dst = st + (size_t)row * w2row + 16 * pc;
       if (p0 + row < hi_u) {
-        const int nid = __ldg(a.uidx + p0 + row);
+        const int nid = a.dense ? p0 + row : __ldg(a.uidx + p0 + row);
         cp_async16(dst, w2base + (size_t)nid * w2s + c0 + 8 * pc);
       } else {
         *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);

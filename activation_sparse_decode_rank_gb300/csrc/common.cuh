@@ -144,6 +144,11 @@ __device__ __forceinline__ void compute_sync() {
 }
 
 // Makes mbarrier initialisation visible to the asynchronous (TMA) proxy.
+// Invalidates an mbarrier so that its memory may be initialised again (no
+// arrival or transaction may be pending on it).
+__device__ __forceinline__ void mbar_inval(uint64_t* m) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(m)) : "memory");
+}
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

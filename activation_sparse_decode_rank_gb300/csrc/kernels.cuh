@@ -129,34 +129,73 @@ __device__ __forceinline__ void prefetch_neuron(const FfnArgs& a, int i) {
 }
 
 // ------------------------------------------------------------ predictor (fused)
-// Logits of this block's own neurons i = c + j P (j < rows), four lanes per
-// row, eight rows per warp at a time; flag[j] = (logit > 0).
-template <int DT>
+// Logits of this block's own neurons i = c + j P (j < rows); flag[j] =
+// (logit > 0).  A row is rc = r / 8 sixteen-byte pieces.
+//   Rows staged in shared memory: four lanes per row, eight rows per warp at
+//   a time, each lane summing its pieces l, l + 4, ...
+//   Rows read through L2: RC lanes (the power of two >= rc) take one row, so
+//   one warp load covers 32 / RC rows, and each lane keeps up to NB row
+//   loads in flight before the first use.
+// A row's lane sums meet in a fixed shuffle tree.
+template <int DT, int NB = 12>
 __device__ void own_logits(const FfnArgs& a, const unsigned char* As, const float* b1s,
                            const float* us, unsigned char* flag, int rows) {
   const int rc = a.r >> 3;
+  if (a.a_in_smem) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, l = lane & 3;
+    for (int base = warp * 8; base < rows; base += kWarps * 8) {
+      const int j = base + g;
+      float acc = 0.f;
+      if (j < rows) {
+        for (int q = l; q < rc; q += 4) {
+          float f[8], u[8];
+          unpack8<DT>(*reinterpret_cast<const uint4*>(As + (size_t)j * a.a_stride + 16 * q), f);
+          load8(us + 8 * q, u);
+          acc += dot8(f, u);
+        }
+      }
+      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+      if (j < rows && l == 0) flag[j] = (acc + b1s[j] > 0.f) ? 1 : 0;
+    }
+    return;
+  }
+  int RC = 1;
+  while (RC < rc) RC <<= 1;
+  const int per = 32 / RC;
   const int c = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, l = lane & 3;
-  for (int base = warp * 8; base < rows; base += kWarps * 8) {
-    const int j = base + g;
-    float acc = 0.f;
-    if (j < rows) {
-      for (int q = l; q < rc; q += 4) {
-        uint4 v;
-        if (a.a_in_smem)
-          v = *reinterpret_cast<const uint4*>(As + (size_t)j * a.a_stride + 16 * q);
-        else
-          v = ld_nc(a.A + ((size_t)c + (size_t)j * a.P) * a.r + 8 * q);
-        float f[8], u[8];
-        unpack8<DT>(v, f);
-        load8(us + 8 * q, u);
-        acc += dot8(f, u);
-      }
+  const int sub = lane / RC, l = lane - sub * RC;
+  const bool lane_ok = l < rc;
+  float u[8];
+  if (lane_ok) {
+    load8(us + 8 * l, u);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) u[e] = 0.f;
+  }
+  const int stride = kWarps * per;  // rows of one block-wide load round
+  for (int b0 = warp * per; b0 < rows; b0 += NB * stride) {  // warp-uniform
+    uint4 v[NB];
+#pragma unroll
+    for (int t = 0; t < NB; ++t) {
+      const int j = b0 + sub + t * stride;
+      if (lane_ok && j < rows) v[t] = ld_nc(a.A + ((size_t)c + (size_t)j * a.P) * a.r + 8 * l);
     }
-    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-    if (j < rows && l == 0) flag[j] = (acc + b1s[j] > 0.f) ? 1 : 0;
+#pragma unroll
+    for (int t = 0; t < NB; ++t) {
+      const int j = b0 + sub + t * stride;
+      if (b0 + t * stride >= rows) break;  // warp-uniform: no row of this round left
+      float acc = 0.f;
+      if (lane_ok && j < rows) {
+        float f[8];
+        unpack8<DT>(v[t], f);
+        acc = dot8(f, u);
+      }
+      for (int o = RC >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (l == 0 && j < rows) flag[j] = (acc + b1s[j] > 0.f) ? 1 : 0;
+    }
   }
 }
 
@@ -323,19 +362,21 @@ __device__ void final_reduce(const FfnArgs& a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int D4 = a.d >> 2;
   const int j0 = (int)((long long)c * D4 / P), j1 = (int)((long long)(c + 1) * D4 / P);
-  constexpr int PU = kPMax / 32;
+  constexpr int PU = 6;  // loads in flight per lane (one batch up to 192 blocks)
   for (int j = j0 + warp; j < j1; j += kWarps) {
-    float4 v[PU];
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p0 = 0; p0 < P; p0 += 32 * PU) {
+      float4 v[PU];
 #pragma unroll
-    for (int u = 0; u < PU; ++u) {
-      const int p = lane + 32 * u;
-      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (p < P) v[u] = __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)p * a.d) + j);
-    }
-    float4 s = v[0];
+      for (int u = 0; u < PU; ++u) {
+        const int p = p0 + lane + 32 * u;
+        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (p < P) v[u] = __ldcg(reinterpret_cast<const float4*>(a.part + (size_t)p * a.d) + j);
+      }
 #pragma unroll
-    for (int u = 1; u < PU; ++u) {
-      s.x += v[u].x; s.y += v[u].y; s.z += v[u].z; s.w += v[u].w;
+      for (int u = 0; u < PU; ++u) {
+        s.x += v[u].x; s.y += v[u].y; s.z += v[u].z; s.w += v[u].w;
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {

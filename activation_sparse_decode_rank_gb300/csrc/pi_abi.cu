@@ -10,6 +10,7 @@
 
 #include "kernels.cuh"
 #include "batched.cuh"
+#include "seq.cuh"
 
 using namespace pik;
 
@@ -24,6 +25,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // Byte offsets of the workspace regions.
 struct WsLayout {
   size_t ctrl, upart, loc_tot, mask, part, u, logits, total;
+  size_t uacc;  // sequence kernel: 2 x r fixed-point accumulators, one 128-byte line each
   // batched path (batch > 1)
   size_t bidx, bcnt, uidx, ucnt, tmask, xhi, xlo, hhi, hlo, bpart;
   int bp, hs;
@@ -41,12 +43,14 @@ WsLayout ws_layout(const pi_ffn_desc& D, int batch) {
     return o;
   };
   L.ctrl = take(256);  // grid barrier arrival counter (64-bit)
-  L.upart = take(sizeof(float) * (size_t)D.r * kSMax);
+  // predictor partials: r x kSMax (one-layer kernel) or r x P (sequence kernel)
+  L.upart = take(sizeof(float) * (size_t)D.r * (kPMax > kSMax ? kPMax : kSMax));
   L.loc_tot = take(sizeof(int) * kPMax);
   L.mask = take((size_t)D.n);
   L.part = take(sizeof(float) * (size_t)kPMax * D.d);
   L.u = take(sizeof(float) * (size_t)batch * D.r);
   L.logits = take(sizeof(float) * (size_t)batch * D.n);
+  L.uacc = take(2 * 128 * (size_t)D.r);
   L.bp = batch_pad(batch);
   L.hs = h_stride(D.n);
   if (batch > 1) {
@@ -312,6 +316,7 @@ void bind_weights(FfnArgs& a, const pi_layer_weights& w) {
 // ------------------------------------------------------------ batched path
 // The three tensor-core phases of a batched sparse FFN over the union of the
 // tokens' active neurons (uidx / ucnt / tmask in device memory).
+// uidx == NULL: the dense batched FFN (all n neurons, every token).
 pi_status launch_batched(const pi_ffn_desc& D, const pi_layer_weights& w, const float* x,
                          int batch, const int* uidx, const int* ucnt, const uint32_t* tmask,
                          float* y, const float* residual, const WsLayout& L, void* ws,
@@ -340,6 +345,7 @@ pi_status launch_batched(const pi_ffn_desc& D, const pi_layer_weights& w, const 
   a.uidx = uidx;
   a.ucnt = ucnt;
   a.tmask = tmask;
+  a.dense = uidx == nullptr;
   a.xhi = reinterpret_cast<uint16_t*>(b + L.xhi);
   a.xlo = reinterpret_cast<uint16_t*>(b + L.xlo);
   a.hhi = reinterpret_cast<uint16_t*>(b + L.hhi);
@@ -418,7 +424,8 @@ WsLayout static_layout(const pi_ffn_desc& D, int P) {
     return o;
   };
   L.ctrl = take(256);
-  L.upart = take(sizeof(float) * (size_t)D.r * kSMax);
+  // predictor partials: r x kSMax (one-layer kernel) or r x P (sequence kernel)
+  L.upart = take(sizeof(float) * (size_t)D.r * (kPMax > kSMax ? kPMax : kSMax));
   L.loc_tot = take(sizeof(int) * (size_t)P);
   L.mask = take((size_t)D.n);
   L.part = take(sizeof(float) * (size_t)P * D.d);
@@ -428,6 +435,17 @@ WsLayout static_layout(const pi_ffn_desc& D, int P) {
 }
 
 }  // namespace
+
+// ------------------------------------------------------------ layer sequence
+using SeqFn = void (*)(const SeqArgs);
+SeqFn pick_seq(int dtype, int gated, bool wide) {
+  if (dtype == PI_F16) {
+    if (!gated) return wide ? seq_kernel<0, false, 2> : seq_kernel<0, false, 1>;
+    return wide ? seq_kernel<0, true, 2> : seq_kernel<0, true, 1>;
+  }
+  if (!gated) return wide ? seq_kernel<1, false, 2> : seq_kernel<1, false, 1>;
+  return wide ? seq_kernel<1, true, 2> : seq_kernel<1, true, 1>;
+}
 
 extern "C" {
 
@@ -487,6 +505,7 @@ const char* pi_status_string(pi_status s) {
     case PI_ERR_TIMEOUT: return "a bounded grid-wide wait ran out";
     case PI_ERR_CUDA: return "a CUDA runtime call failed";
     case PI_ERR_INDEX: return "an active-list entry is outside [0, n)";
+    case PI_ERR_RANGE: return "a predictor partial sum is outside the fixed-point range";
   }
   return "unknown status";
 }
@@ -617,6 +636,9 @@ pi_status pi_dense_ffn(const pi_ffn_desc* desc, const pi_layer_weights* w, const
     if (!aligned16(p)) return PI_ERR_ALIGN;
   const WsLayout L = ws_layout(*desc, batch);
   if (ws_bytes < L.total) return PI_ERR_WORKSPACE;
+  if (batch > 1 && desc->d % kBK == 0)  // every row read once for all tokens, tensor cores
+    return launch_batched(*desc, *w, x, batch, nullptr, nullptr, nullptr, y, nullptr, L, ws,
+                          reinterpret_cast<cudaStream_t>(stream));
   for (int t = 0; t < batch; ++t) {
     FfnArgs a{};
     bind_weights(a, *w);
@@ -680,6 +702,100 @@ pi_status pi_layer_decode(const pi_ffn_desc* desc, const pi_layer_weights* w, co
     if (s != PI_OK) return s;
   }
   return PI_OK;
+}
+
+pi_status pi_decode_layers(const pi_ffn_desc* descs, const pi_layer_weights* layers, int32_t R,
+                           int32_t J, const float* x, int32_t chain, float* y, int32_t* cnt_out,
+                           uint8_t* mask_out, int32_t* dev_status, void* ws, size_t ws_bytes,
+                           pi_stream stream) {
+  if (!descs || !layers) return PI_ERR_NULL;
+  if (R < 1 || R > kSeqMaxLayers || J < 1 || (chain != 0 && chain != 1)) return PI_ERR_SHAPE;
+  pi_ffn_desc D = descs[0];
+  int hot_max = 0;
+  for (int l = 0; l < R; ++l) {
+    const pi_ffn_desc& E = descs[l];
+    pi_status s = check_desc(&E);
+    if (s != PI_OK) return s;
+    if (E.d != D.d || E.n != D.n || E.r != D.r || E.dtype != D.dtype || E.gated != D.gated ||
+        E.layout != D.layout)
+      return PI_ERR_SHAPE;
+    s = check_weights(E, &layers[l], true);
+    if (s != PI_OK) return s;
+    if (E.hot_prefix > hot_max) hot_max = E.hot_prefix;
+  }
+  if (!x || !y || !dev_status || !ws) return PI_ERR_NULL;
+  const void* ps[] = {x, y, cnt_out, dev_status, ws};
+  for (const void* p : ps)
+    if (p && !aligned16(p)) return PI_ERR_ALIGN;
+  const WsLayout L = ws_layout(D, 1);
+  if (ws_bytes < L.total) return PI_ERR_WORKSPACE;
+  DevInfo di;
+  pi_status s = dev_info(&di);
+  if (s != PI_OK) return s;
+  const int P = di.sms < kPMax ? di.sms : kPMax;
+  if ((D.d / 8 + P - 1) / P > kSeqMaxQ) return PI_ERR_SHAPE;  // own columns per block
+  D.hot_prefix = hot_max;
+  const bool wide = (D.d / 8) > kThreads;
+  SeqFn fn = pick_seq(D.dtype, D.gated, wide);
+  FfnArgs a{};
+  const int smem = plan_ffn(D, kFused, P, D.n, di.smem_optin - 1024, a);
+  if (smem == 0 || a.grp < 1) return PI_ERR_SHAPE;
+  s = ensure_smem(reinterpret_cast<const void*>(fn), smem);
+  if (s != PI_OK) return s;
+  bind_ws(a, L, ws);
+  a.mask = nullptr;
+  a.idx_out = nullptr;
+  a.cnt_out = nullptr;
+  a.status = dev_status;
+  a.limit_ns = wait_limit_ns();
+  SeqArgs sa{};
+  sa.f = a;
+  sa.J = J;
+  sa.R = R;
+  sa.chain = chain;
+  sa.x = x;
+  sa.y = y;
+  sa.cnt_out = cnt_out;
+  sa.mask_out = mask_out;
+  sa.uacc = reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) + L.uacc);
+  const int qmax = (D.d / 8 + P - 1) / P;
+  sa.bm_smem = (a.nh < a.ns - 1 && D.r * qmax * 16 <= a.slot_bytes) ? 1 : 0;
+  for (int l = 0; l < R; ++l) {
+    const pi_layer_weights& w = layers[l];
+    SeqLayer& e = sa.L[l];
+    e.A = static_cast<const uint16_t*>(w.A);
+    e.Bm = static_cast<const uint16_t*>(w.Bm);
+    e.b1 = w.b1;
+    e.W1 = static_cast<const uint16_t*>(w.W1);
+    e.W2 = static_cast<const uint16_t*>(w.W2);  // NULL when packed (records hold both)
+    e.b2 = w.b2;
+    e.hot = descs[l].hot_prefix;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)P);
+  cfg.blockDim = dim3(kBlock);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  if (launch_mode() == 0) {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  } else {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kBlock, (size_t)smem) !=
+        cudaSuccess)
+      return PI_ERR_CUDA;
+    if (per_sm < 1) return PI_ERR_LAUNCH;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // the fixed-point u accumulators start at zero (the kernel keeps them so
+  // between its jobs)
+  if (cudaMemsetAsync(sa.uacc, 0, 2 * 128 * (size_t)D.r, cfg.stream) != cudaSuccess)
+    return PI_ERR_CUDA;
+  return map_launch_error(cudaLaunchKernelEx(&cfg, fn, sa));
 }
 
 pi_status pi_pack_weights(const pi_ffn_desc* desc, const void* W1, const void* W2, void* packed,

@@ -1,0 +1,339 @@
+// seq.cuh — decode through a sequence of FFN layers in one persistent launch.
+//
+// Same method as the one-layer kernel (predictor, mask, hot-first row
+// gather, row-axpy, fixed-order split reduction; "PowerInfer: Quick Massive
+// Language Mannequin Serving with a Client-grade GPU", sections "Online
+// Section" and "Neuron Conscious Operator"), run for J jobs in a row.  Job j
+// uses layer table entry j % R; chained jobs form a residual stack
+// (x_{j+1} = x_j + FFN_j(x_j)), independent jobs read their own x.
+//
+// Two grid-wide waits per job.  Block c owns the 8-column chunks
+// [c nch / P, (c+1) nch / P) of the layer's d columns:
+//   R  after the previous job's partial rows are complete: the block sums
+//      its columns of the P partials (fixed order), adds b2 and the residual
+//      and writes them (chained: its columns of the next x);
+//   U  predictor stage 1 over its own columns only (split-K): a partial u
+//      of r values per block, so no block needs the whole new x yet.  The
+//      partials meet in 64-bit fixed-point accumulators (value x 2^32,
+//      integer reductions in memory): integer addition is associative, so
+//      u is the same whatever order the blocks arrive in (deterministic),
+//      and it is exact up to the one rounding of each partial to 2^-32;
+//   -- wait 1 --
+//   L  full x and u, logits of the block's own neurons, their ordered
+//      active list;
+//      ring: the row-gather GEMV + ReLU and row-axpy of those neurons;
+//      then the next job's weights that do not depend on its x (the own hot
+//      neurons' rows into ring slots, the rest of the hot rows and the
+//      predictor rows towards L2 / shared memory) are requested, so that
+//      their transfer overlaps this job's tail;
+//   -- wait 2 -- (partial rows written)
+// A job's x is read only after the previous job is complete: jobs never
+// overlap in anything that depends on their inputs.
+#pragma once
+
+#include "kernels.cuh"
+
+namespace pik {
+
+constexpr int kSeqMaxLayers = 128;
+constexpr int kSeqMaxQ = 8;  // most own 8-column chunks per block
+
+struct SeqLayer {
+  const uint16_t* A;
+  const uint16_t* Bm;
+  const float* b1;
+  const uint16_t* W1;
+  const uint16_t* W2;
+  const float* b2;
+  int hot;
+  int pad_;
+};
+
+struct SeqArgs {
+  FfnArgs f;              // shape, grid, shared-memory plan, workspace (weights per job)
+  int J, R, chain;
+  const float* x;         // chained: [d]; else [J][d]
+  float* y;               // [J][d] (chained: x_{j+1})
+  int* cnt_out;           // [J] or NULL
+  unsigned char* mask_out;  // [J][n] or NULL
+  unsigned long long* uacc;  // [2][r] fixed-point u, 16 words (128 bytes) apart; zero at launch
+  int bm_smem;            // stage the next job's own Bm columns in the last ring slot
+  SeqLayer L[kSeqMaxLayers];
+};
+
+template <int DT, bool GATED, int NCH>
+__global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const FfnArgs& f = sa.f;
+  float* xs = reinterpret_cast<float*>(smem + f.o_xs);
+  int* lst = reinterpret_cast<int*>(smem + f.o_lst);
+  float* lb = reinterpret_cast<float*>(smem + f.o_lb);
+  float* red = reinterpret_cast<float*>(smem + f.o_red);
+  float* xo = red + 2 * kGroup * 2 * kWarps + 2 * kGroup;  // own x columns (<= 64 floats)
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + f.o_mbar);
+  uint64_t* empty = full + kMaxSlots;
+  unsigned char* slots = smem + f.o_slots;
+  unsigned char* As = smem + f.o_As;
+  float* b1s = reinterpret_cast<float*>(smem + f.o_b1s);
+  float* us = reinterpret_cast<float*>(smem + f.o_us);
+  unsigned char* flag = smem + f.o_flag;
+  const int c = blockIdx.x, P = f.P;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool compute = tid < kThreads;
+  __shared__ int s_m, s_mh, s_bad;
+  __shared__ unsigned long long s_base;
+
+  const int rows = (c < f.n) ? (f.n - 1 - c) / P + 1 : 0;  // own neurons c, c + P, ...
+  const int q0 = (int)((long long)c * f.nch / P), q1 = (int)((long long)(c + 1) * f.nch / P);
+  const int nq = q1 - q0;  // own 8-column chunks (<= kSeqMaxQ, checked by the host)
+  const int rc = f.r >> 3;
+
+  unsigned char* bms = slots + (size_t)(f.ns - 1) * f.slot_bytes;  // staged Bm columns
+  FfnArgs a = f;  // the current job's weights
+  int nh_c = 0;   // own hot neurons whose rows went to slots for the current job
+
+  // Requests the weights of job j that do not depend on its x.  No copy may
+  // be in flight (the ring barriers are re-armed).
+  bool armed = false;  // the ring barriers hold a previous job's state
+  auto prep = [&](int j) {
+    const SeqLayer& Lw = sa.L[j % sa.R];
+    a.A = Lw.A;
+    a.Bm = Lw.Bm;
+    a.b1 = Lw.b1;
+    a.W1 = Lw.W1;
+    a.W2 = Lw.W2;
+    a.b2 = Lw.b2;
+    a.hot = Lw.hot;
+    const int hot_own = (c < a.hot) ? (a.hot - 1 - c) / P + 1 : 0;
+    nh_c = min(f.nh, hot_own);
+    if (tid == 0) {
+      for (int s = 0; s < f.ns; ++s) {
+        if (armed) {
+          mbar_inval(full + s);
+          mbar_inval(empty + s);
+        }
+        mbar_init(full + s, 1u);
+        mbar_init(empty + s, (unsigned)kWarps);
+      }
+      fence_mbar_init();
+      for (int k = 0; k < nh_c; ++k) issue_neuron<GATED>(a, slots, full, k, c + k * P);
+    }
+    armed = true;
+    if (compute) {
+      // the small copies the next phases wait for go out first: own Bm
+      // columns ([k][q], 16 bytes each, into the last ring slot, a cold one),
+      // biases, staged predictor rows; then the predictor rows towards L2
+      if (sa.bm_smem)
+        for (int e = tid; e < f.r * nq; e += kThreads) {
+          const int k = e / nq, q = e - k * nq;
+          cp_async16(bms + (size_t)e * 16, a.Bm + (size_t)k * f.d + 8 * (q0 + q));
+        }
+      for (int jj = tid; jj < rows; jj += kThreads) cp_async4(b1s + jj, a.b1 + c + (size_t)jj * P);
+      if (f.a_in_smem)
+        for (int e = tid; e < rows * rc; e += kThreads) {
+          const int jj = e / rc, q = e - jj * rc;
+          cp_async16(As + (size_t)jj * f.a_stride + 16 * q,
+                     a.A + ((size_t)c + (size_t)jj * P) * f.r + 8 * q);
+        }
+      cp_async_commit();
+      if (!f.a_in_smem)
+        for (int jj = tid; jj < rows; jj += kThreads)
+          prefetch_l2(a.A + ((size_t)c + (size_t)jj * P) * f.r, (size_t)f.r * 2);
+      // the own hot neurons beyond the slots, towards L2
+      for (int k = nh_c + tid; k < hot_own; k += kThreads) prefetch_neuron<GATED>(a, c + k * P);
+    }
+  };
+  // On a failed grid-wide wait: let this block's own copies land, then leave.
+  auto bail = [&]() {
+    cp_async_wait_all();
+    if (tid == kThreads)
+      for (int k = 0; k < nh_c; ++k) mbar_wait(full + k, 0u, f.limit_ns);
+    __syncthreads();
+  };
+
+  if (tid == 0) s_bad = 0;
+  prep(0);
+  pdl_wait();
+  if (tid == 0) s_base = grid_base(f.bar, (unsigned)P);
+  unsigned long long nbar = 0;
+
+  for (int j = 0; j < sa.J; ++j) {
+    // own columns of this job's x: job 0 reads them here; later jobs find
+    // them in xo (written by the previous job's R phase)
+    if (j == 0 && tid < nq * 8) xo[tid] = __ldcg(sa.x + 8 * q0 + tid);
+    cp_async_wait_all();  // this job's staged weights
+    __syncthreads();
+    // U: partial predictor stage 1 over the own columns, u_c[k] for k < r
+    if (tid < f.r) {
+      const uint16_t* row = a.Bm + (size_t)tid * f.d + 8 * q0;
+      float acc = 0.f;
+      for (int qb = 0; qb < nq; qb += 4) {  // batches of 4 pieces, loads first
+        uint4 wv[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          if (qb + t < nq)
+            wv[t] = sa.bm_smem
+                        ? *reinterpret_cast<const uint4*>(bms + ((size_t)tid * nq + qb + t) * 16)
+                        : ld_nc(row + 8 * (qb + t));
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          if (qb + t < nq) {
+            float w[8], xv[8];
+            unpack8<DT>(wv[t], w);
+            load8(xo + 8 * (qb + t), xv);
+            acc += dot8(w, xv);
+          }
+        }
+      }
+      if (!(fabsf(acc) < 8388608.f)) {  // |partial| >= 2^23, or NaN
+        set_status(f.status, PI_ERR_RANGE);
+        acc = 0.f;
+      }
+      const long long v = __double2ll_rn((double)acc * 4294967296.0);
+      unsigned long long* dst = sa.uacc + ((size_t)(j & 1) * f.r + tid) * 16;
+      asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(dst), "l"((unsigned long long)v)
+                   : "memory");
+    }
+    ++nbar;
+    if (!grid_sync(f.bar, s_base + nbar * P, f.status, f.limit_ns)) {
+      bail();
+      return;
+    }
+    // L: the whole x, u, own logits and list
+    const float* xj = sa.chain ? (j == 0 ? sa.x : sa.y + (size_t)(j - 1) * f.d)
+                               : sa.x + (size_t)j * f.d;
+    for (int i = tid; i < (f.d >> 2); i += kBlock)
+      reinterpret_cast<float4*>(xs)[i] = __ldcg(reinterpret_cast<const float4*>(xj) + i);
+    if (tid < f.r) {
+      // u[k] from its accumulator; block 0 clears the other buffer (last
+      // read by the previous job, before this job's first wait) for the next
+      const unsigned long long v = __ldcg(sa.uacc + ((size_t)(j & 1) * f.r + tid) * 16);
+      us[tid] = (float)((double)(long long)v * 2.3283064365386963e-10);  // x 2^-32
+      if (c == 0) sa.uacc[((size_t)((j + 1) & 1) * f.r + tid) * 16] = 0ull;
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    if (compute) own_logits<DT, 6>(a, As, b1s, us, flag, rows);
+    __syncthreads();
+    if (warp == 0) {
+      unsigned char* mrow = sa.mask_out ? sa.mask_out + (size_t)j * f.n : nullptr;
+      int cnt = 0, nhot = 0;
+      for (int base = 0; base < rows; base += 32) {
+        const int jj = base + lane;
+        const bool fl = (jj < rows) && flag[jj];
+        const unsigned bal = __ballot_sync(0xffffffffu, fl);
+        const int pos = cnt + __popc(bal & ((1u << lane) - 1u));
+        if (fl) {
+          lst[pos] = c + jj * P;
+          lb[pos] = b1s[jj];
+        }
+        if (mrow && jj < rows) mrow[(size_t)c + (size_t)jj * P] = fl ? 1 : 0;
+        cnt += __popc(bal);
+        nhot += __popc(__ballot_sync(0xffffffffu, fl && jj < nh_c));
+      }
+      if (lane == 0) {
+        s_m = cnt;
+        s_mh = nhot;
+        __stcg(f.loc_tot + c, cnt);
+      }
+    }
+    __syncthreads();
+    const int m = s_m, mh = s_mh;
+    float yacc[NCH][8];
+#pragma unroll
+    for (int q = 0; q < NCH; ++q)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) yacc[q][e] = 0.f;
+    ffn_ring<DT, GATED, NCH>(a, xs, lst, lb, m, mh, f.nh, slots, full, empty, red,
+                             red + 2 * kGroup * 2 * kWarps, yacc, &s_bad);
+    __syncthreads();
+    // copies of own hot neurons that turned out inactive land before the
+    // slots are re-armed
+    if (tid == kThreads && mh < nh_c) {
+      for (int k = 0; k < nh_c; ++k) {
+        bool used = false;
+        for (int e = 0; e < mh; ++e) used |= (lst[e] == c + k * P);
+        if (!used && !mbar_wait(full + k, 0u, f.limit_ns)) set_status(f.status, PI_ERR_TIMEOUT);
+      }
+    }
+    __syncthreads();
+    const float* b2j = a.b2;
+    if (compute) {  // the partial rows go out first: wait 2 fences them
+#pragma unroll
+      for (int q = 0; q < NCH; ++q) {
+        const int cc = tid + q * kThreads;
+        if (cc < f.nch) {
+          float4* dst = reinterpret_cast<float4*>(f.part + (size_t)c * f.d + 8 * (size_t)cc);
+          __stcg(dst, make_float4(yacc[q][0], yacc[q][1], yacc[q][2], yacc[q][3]));
+          __stcg(dst + 1, make_float4(yacc[q][4], yacc[q][5], yacc[q][6], yacc[q][7]));
+        }
+      }
+    }
+    if (j + 1 < sa.J) prep(j + 1);  // overlaps wait 2 and R
+    ++nbar;
+    if (!grid_sync(f.bar, s_base + nbar * P, f.status, f.limit_ns)) {
+      bail();
+      return;
+    }
+    if (j + 1 == sa.J) pdl_trigger();  // no grid-wide wait is left
+    if (!sa.chain && j + 1 < sa.J && tid < nq * 8)  // the next step's own columns
+      xo[tid] = __ldcg(sa.x + (size_t)(j + 1) * f.d + 8 * q0 + tid);
+    if (sa.cnt_out && c == 0 && warp == 0) {
+      int sum = 0;
+      for (int b = lane; b < P; b += 32) sum += __ldcg(f.loc_tot + b);
+      sum = __reduce_add_sync(0xffffffffu, sum);
+      if (lane == 0) sa.cnt_out[j] = sum;
+    }
+    // R: own columns of y_j, one float4 column per compute warp: lane l
+    // sums partials l, l + 32, ... (loads issued first), then a fixed
+    // shuffle tree; + b2 (+ the residual x_j when chained)
+    if (warp < 2 * nq) {
+      const int col4 = 2 * q0 + warp;
+      const float4 bb = b2j ? __ldg(reinterpret_cast<const float4*>(b2j) + col4)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+      constexpr int PU = 6;  // loads in flight per lane (one batch up to 192 blocks)
+      float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int p0 = 0; p0 < P; p0 += 32 * PU) {
+        float4 v[PU];
+#pragma unroll
+        for (int u = 0; u < PU; ++u) {
+          const int p = p0 + lane + 32 * u;
+          v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (p < P) v[u] = __ldcg(reinterpret_cast<const float4*>(f.part + (size_t)p * f.d) + col4);
+        }
+#pragma unroll
+        for (int u = 0; u < PU; ++u) {
+          s.x += v[u].x;
+          s.y += v[u].y;
+          s.z += v[u].z;
+          s.w += v[u].w;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        s.x += __shfl_xor_sync(0xffffffffu, s.x, o);
+        s.y += __shfl_xor_sync(0xffffffffu, s.y, o);
+        s.z += __shfl_xor_sync(0xffffffffu, s.z, o);
+        s.w += __shfl_xor_sync(0xffffffffu, s.w, o);
+      }
+      if (lane == 0) {
+        s.x += bb.x;
+        s.y += bb.y;
+        s.z += bb.z;
+        s.w += bb.w;
+        float4* xo4 = reinterpret_cast<float4*>(xo) + warp;
+        if (sa.chain) {
+          const float4 rr = *xo4;  // x_j at these columns
+          s.x += rr.x;
+          s.y += rr.y;
+          s.z += rr.z;
+          s.w += rr.w;
+          *xo4 = s;  // x_{j+1}
+        }
+        reinterpret_cast<float4*>(sa.y + (size_t)j * f.d)[col4] = s;
+      }
+    }
+  }
+}
+
+}  // namespace pik

@@ -265,7 +265,21 @@ def run_ours(args):
     ws = pi.workspace(desc, 1, dev)
     stream = torch.cuda.Stream(device=dev)
 
+    seq = args.engine == "seq"
+    if seq:
+        R = min(R, 128)
+        wts = wts[:R]
+        ys = torch.empty((G, d), dtype=torch.float32, device=dev)
+        cseq = torch.zeros((G + 4,), dtype=torch.int32, device=dev)
+    steps_per_call = G if seq else 1
+
     def step(s, cnt_slot=True, wt=None, xsrc=None, ydst=None):
+        if seq:  # s counts calls; each call decodes G steps in one launch
+            rc = pi.pi_decode_layers([desc] * R, wts, G, xs if xsrc is None else xsrc, 0,
+                                     ys if ydst is None else ydst, cseq if cnt_slot else None,
+                                     None, st, ws, stream=stream)
+            pi.check(rc, "pi_decode_layers")
+            return
         rc = pi.pi_layer_decode(desc, wts[s % R] if wt is None else wt,
                                 xs[s % G] if xsrc is None else xsrc, 1,
                                 y if ydst is None else ydst, None, None,
@@ -280,16 +294,19 @@ def run_ours(args):
                     fn(s)
         return g
 
+    if seq and args.steps % G:
+        raise SystemExit(f"bench: --steps must be a multiple of the graph length {G} (seq engine)")
     with torch.cuda.stream(stream):
-        for s in range(min(G, 8)):   # eager run first: attribute setup, sanity
+        for s in range(1 if seq else min(G, 8)):   # eager run first: attribute setup, sanity
             step(s)
         stream.synchronize()
         if int(st[0]) != 0:
             raise SystemExit(f"bench: device status {pi.status_string(int(st[0]))}")
-    g_main = capture(G, step)
-    tail = args.steps % G
+    calls_per_graph = 1 if seq else G
+    g_main = capture(calls_per_graph, step)
+    tail = 0 if seq else args.steps % G
     g_tail = capture(tail, step) if tail else None
-    g_warm = capture(min(args.warmup, G), step)
+    g_warm = g_main if seq else capture(min(args.warmup, G), step)
 
     def replay_steps(k):
         full, rem = divmod(k, G)
@@ -305,7 +322,7 @@ def run_ours(args):
 
     # warmup (untimed): at least W steps
     with torch.cuda.stream(stream):
-        gw = min(args.warmup, G)
+        gw = G if seq else min(args.warmup, G)
         for _ in range(math.ceil(args.warmup / gw)):
             g_warm.replay()
         stream.synchronize()
@@ -329,7 +346,7 @@ def run_ours(args):
         raise SystemExit(f"bench: device status {pi.status_string(int(st[0]))}")
 
     # byte accounting from the run's own active counts
-    cnt_host = cnts[:, 0].cpu().numpy().astype(np.float64)
+    cnt_host = (cseq[:G] if seq else cnts[:, 0]).cpu().numpy().astype(np.float64)
     mean_cnt = float(cnt_host.mean())
     active_bytes = mean_cnt * m_rows * d * 2
     alg_bytes = pred_bytes + active_bytes
@@ -343,9 +360,10 @@ def run_ours(args):
         ms_all = [float(tt.item())]
     value, t_max = aggregate(ms_all, [args.steps * world], world)
     ms_per_step = t_max / args.steps
-    per_launch_s = ms / args.steps / 1e3
+    launches = args.steps // steps_per_call
+    per_launch_s = ms / launches / 1e3
     peak, peak_kind = measured_peaks()
-    achieved = alg_bytes / per_launch_s / 1e9
+    achieved = alg_bytes * steps_per_call / per_launch_s / 1e9
 
     # dense-FFN comparison point (same replicas, same protocol)
     dense_steps = min(200, args.steps)
@@ -377,16 +395,24 @@ def run_ours(args):
     yh = torch.empty((G, d), dtype=torch.float32).pin_memory()
     xin = torch.empty((1, d), dtype=torch.float32, device=dev)
 
+    if seq:
+        xin_all = torch.empty((G, d), dtype=torch.float32, device=dev)
+
     def estep(s):
+        if seq:  # one call: the chunk's G inputs up, G decode steps, G outputs down
+            xin_all.copy_(xh, non_blocking=True)
+            step(s, cnt_slot=False, xsrc=xin_all)
+            yh.copy_(ys, non_blocking=True)
+            return
         xin.copy_(xh[s % G:s % G + 1], non_blocking=True)
         step(s, cnt_slot=False, xsrc=xin)
         yh[s % G:s % G + 1].copy_(y, non_blocking=True)
 
     with torch.cuda.stream(stream):
-        for s in range(2):
+        for s in range(1 if seq else 2):
             estep(s)
     stream.synchronize()
-    g_e2e = capture(G, estep)
+    g_e2e = capture(calls_per_graph, estep)
     with torch.cuda.stream(stream):
         g_e2e.replay()
         stream.synchronize()
@@ -423,7 +449,7 @@ def run_ours(args):
                "sample": f"first {done} decode steps of {args.workload} (time-bounded at "
                          f"{budget:.0f} s), fp64 oracle predict+compact+sparse FFN"}
 
-    kernel_key = f"ffn_kernel_fused:{args.workload}"
+    kernel_key = (f"seq_kernel:{args.workload}" if seq else f"ffn_kernel_fused:{args.workload}")
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -443,14 +469,16 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": stored_traffic(kernel_key),
                      "peak_kind": f"{peak_kind} copy bandwidth",
-                     "kernel": "ffn_kernel (fused predictor+compaction+FFN, one launch/step)"},
+                     "kernel": (f"seq_kernel (persistent, {G} decode steps per launch)" if seq
+                                else "ffn_kernel (fused predictor+compaction+FFN, one launch/step)")},
         "dense_ffn": {"us_per_step": dense_ms * 1e3, "tokens_per_s": 1e3 / dense_ms,
                       "achieved_gbs": dense_bytes / (dense_ms / 1e3) / 1e9,
                       "frac": dense_bytes / (dense_ms / 1e3) / 1e9 / peak},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": d * 4,
                 "d2h_bytes_per_step": d * 4, "steps": e2e_done,
                 "how": "CUDA-graph replay of (pinned H2D x, pi_layer_decode, D2H y) per step"},
-        "gpu_launches": args.steps,
+        "gpu_launches": launches,
+        "engine": args.engine,
         "clocks": clocks,
         "cpu_baseline": cpu,
         "csrc_hash": csrc_hash(),
@@ -505,11 +533,18 @@ def run_stack(args):
         [synth.gen_x(w["seed"] + 1000 * rank, s, 1, d) for s in range(G)])).to(dev)
     xbuf = torch.empty((L + 1, d), dtype=torch.float32, device=dev)
     cnts = torch.zeros((G, L, 4), dtype=torch.int32, device=dev)
+    cseq = torch.zeros((G, (L + 3) // 4 * 4), dtype=torch.int32, device=dev)  # 16-byte rows
     st = torch.zeros(4, dtype=torch.int32, device=dev)
     ws = pi.workspace(descs[0], 1, dev)
     stream = torch.cuda.Stream(device=dev)
 
+    seq = args.engine == "seq"
+
     def step(s):
+        if seq:  # the whole stack for one token in one persistent launch
+            pi.check(pi.pi_decode_layers(descs, wts, L, xs[s % G], 1, xbuf[1:], cseq[s % G],
+                                         None, st, ws, stream=stream), "pi_decode_layers")
+            return
         for l in range(L):
             xin = xs[s % G] if l == 0 else xbuf[l]
             pi.check(pi.pi_layer_decode(descs[l], wts[l], xin, 1, xbuf[l + 1], xin, None,
@@ -543,7 +578,7 @@ def run_stack(args):
     steps = reps * G
     if int(st[0]) != 0:
         raise SystemExit(f"bench: device status {pi.status_string(int(st[0]))}")
-    mean_cnt = cnts[:, :, 0].float().mean(dim=0).cpu().numpy()
+    mean_cnt = (cseq[:, :L] if seq else cnts[:, :, 0]).float().mean(dim=0).cpu().numpy()
     alg_bytes = pred_bytes + float(mean_cnt.sum()) * 2 * d * 2
     ms_step = ms / steps
     peak, peak_kind = measured_peaks()
@@ -563,9 +598,146 @@ def run_stack(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None,
                      "peak_kind": f"{peak_kind} copy bandwidth"},
-        "gpu_launches": steps * L, "clocks": clocks, "csrc_hash": csrc_hash(),
+        "gpu_launches": steps * (1 if seq else L), "engine": args.engine,
+        "clocks": clocks, "csrc_hash": csrc_hash(),
     }
     print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_sweep(args):
+    """Batched decode and density sweep (one JSON line, one entry per point):
+    for each mean per-token density and batch B, one step = B tokens (each
+    with its own x and its own predicted mask) through pi_layer_decode, the
+    union of the tokens' active rows read once; the dense FFN at the same
+    batch (pi_dense_ffn: every row read once for all B tokens) is the
+    comparison point.  Two weight replicas alternate between steps."""
+    import torch
+
+    import activation_sparse_decode_rank_gb300 as pi
+    import synth
+
+    rank, world, local = dist_env()
+    if rank != 0:
+        return 0
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pi.build()
+    from synth.workloads import WORKLOADS
+    w = dict(WORKLOADS[args.workload])
+    d, n, r = w["d"], w["n"], w["r"]
+    K = max(20, min(args.steps, 400))
+    G = 64
+    pred_bytes = n * r * 2 + r * d * 2 + n * 4
+    row_bytes = 2 * d * 2
+    stream = torch.cuda.Stream(device=dev)
+    points = []
+    sampler = ClockSampler(local)
+    sampler.start()
+    for rho in w["densities"]:
+        g = synth.make_layer_gpu(d, n, r, w["dtype"], alpha=w["alpha"], density=rho,
+                                 seed=w["seed"], device=dev)
+        pz = synth.zipf_probs(n, w["alpha"], synth.zipf_calibrate(n, w["alpha"], rho))
+        hot = int((pz >= 0.5).sum()) if args.hot < 0 else args.hot
+        desc = pi.make_desc(d, n, r, w["dtype"], False, hot, packed=True)
+        rec = torch.empty((n, 2 * d), dtype=torch.int16, device=dev)
+        pi.check(pi.pi_pack_weights(desc, g["W1"], g["W2"], rec), "pi_pack_weights")
+        torch.cuda.synchronize()
+        base = [g["A"], g["Bm"], g["b1"], rec, None, g["b2"]]
+        reps = [base, [t.clone() if t is not None else None for t in base]]
+        del g
+        wts = [pi.make_weights(*rp) for rp in reps]
+        for B in w["batches"]:
+            xs = torch.from_numpy(np.stack(
+                [synth.gen_x(w["seed"] + 100 * B, s, B, d) for s in range(G)])).to(dev)
+            y = torch.empty((B, d), dtype=torch.float32, device=dev)
+            st = torch.zeros(4, dtype=torch.int32, device=dev)
+            ws = pi.workspace(desc, B, dev)
+            cnt = torch.zeros((max(B, 4),), dtype=torch.int32, device=dev)
+
+            def sp(s):
+                pi.check(pi.pi_layer_decode(desc, wts[s % 2], xs[s % G], B, y, None, None, None,
+                                            st, ws, stream=stream), "pi_layer_decode")
+
+            def dn(s):
+                pi.check(pi.pi_dense_ffn(desc, wts[s % 2], xs[s % G], B, y, ws, stream=stream),
+                         "pi_dense_ffn")
+
+            res = {}
+            for name, fn in (("sparse", sp), ("dense", dn)):
+                with torch.cuda.stream(stream):
+                    for s in range(3):
+                        fn(s)
+                    stream.synchronize()
+                    gr = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(gr, stream=stream):
+                        for s in range(K):
+                            fn(s)
+                    gr.replay()
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    gr.replay()
+                    e1.record(stream)
+                    stream.synchronize()
+                res[name] = e0.elapsed_time(e1) / K * 1e3  # us per step
+                del gr
+            if int(st[0]) != 0:
+                raise SystemExit(f"bench: device status {pi.status_string(int(st[0]))}")
+            # union sizes and per-token counts of the timed inputs (same kernels)
+            logits = torch.empty((B, n), dtype=torch.float32, device=dev)
+            idx = torch.empty((B, n), dtype=torch.int32, device=dev)
+            uidx = torch.empty((n,), dtype=torch.int32, device=dev)
+            ucnt = torch.zeros((4,), dtype=torch.int32, device=dev)
+            tm = torch.empty((n,), dtype=torch.int32, device=dev)
+            us, per_tok = [], []
+            for s in range(0, G, 4):
+                pi.check(pi.pi_predict(desc, reps[0][0], reps[0][1], reps[0][2], xs[s], B, logits,
+                                       ws))
+                pi.check(pi.pi_compact(logits, n, B, idx, cnt, n, uidx, ucnt, tm, st, ws))
+                torch.cuda.synchronize()
+                us.append(int(ucnt[0]))
+                per_tok.append(float(cnt[:B].float().mean()))
+            u_mean = float(np.mean(us))
+            alg = pred_bytes + u_mean * row_bytes
+            dense_alg = n * row_bytes + n * 4
+            peak, _ = measured_peaks()
+            points.append({
+                "density": rho, "batch": B, "per_token_density": float(np.mean(per_tok)) / n,
+                "union_density": u_mean / n,
+                "sparse_us": res["sparse"], "dense_us": res["dense"],
+                "sparse_tokens_per_s": B / res["sparse"] * 1e6,
+                "dense_tokens_per_s": B / res["dense"] * 1e6,
+                "speedup_vs_dense": res["dense"] / res["sparse"],
+                "sparse_gbs": alg / res["sparse"] / 1e3, "sparse_frac": alg / res["sparse"] / 1e3 / peak,
+                "dense_gbs": dense_alg / res["dense"] / 1e3,
+                "dense_frac": dense_alg / res["dense"] / 1e3 / peak,
+            })
+            del xs, ws
+        del reps, wts, base
+        torch.cuda.empty_cache()
+    clocks = sampler.stop()
+    cross = {}
+    for B in w["batches"]:
+        pts = sorted([p for p in points if p["batch"] == B], key=lambda p: p["density"])
+        c = None
+        for p0, p1 in zip(pts, pts[1:]):
+            if p0["speedup_vs_dense"] >= 1.0 > p1["speedup_vs_dense"]:
+                # log-linear interpolation of the speedup between the two densities
+                a0, a1 = math.log(p0["speedup_vs_dense"]), math.log(p1["speedup_vs_dense"])
+                c = p0["density"] + (p1["density"] - p0["density"]) * a0 / (a0 - a1)
+        if c is None and pts and pts[-1]["speedup_vs_dense"] >= 1.0:
+            c = f"> {pts[-1]['density']}"
+        cross[str(B)] = c
+    peak, peak_kind = measured_peaks()
+    print(json.dumps({
+        "metric": "batched sparse-FFN decode: us per step and tokens/s vs the dense FFN",
+        "workload": args.workload, "steps_per_point": K, "unit": "us",
+        "config": {"d": d, "n": n, "r": r, "weights": w["dtype"], "layout": "packed",
+                   "l2": "2 alternating weight replicas of 0.43 GB each"},
+        "peak_gbs": peak, "peak_kind": peak_kind, "points": points,
+        "crossover_density_per_batch": cross, "clocks": clocks, "csrc_hash": csrc_hash(),
+    }), flush=True)
     return 0
 
 
@@ -582,11 +754,18 @@ def main():
     ap.add_argument("--graph-len", type=int, default=2000)
     ap.add_argument("--e2e-steps", type=int, default=20000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--engine", default="call", choices=["call", "seq"],
+                    help="call: one pi_layer_decode launch per step; seq: pi_decode_layers, "
+                         "one persistent launch per graph-length chunk of steps")
+    ap.add_argument("--sweep", action="store_true",
+                    help="batched decode / density sweep (with --workload opt13b_ffn_batched_...)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("bench: at least 3 warm-up steps")
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
     if workload_spec(args.workload).get("layers", 1) > 1:
         return run_stack(args)
     return run_ours(args)

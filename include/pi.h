@@ -75,7 +75,9 @@ typedef enum {
   PI_ERR_LAUNCH = 7,     /* the persistent grid cannot be co-resident          */
   PI_ERR_TIMEOUT = 8,    /* device: a bounded grid-wide wait ran out           */
   PI_ERR_CUDA = 9,       /* a CUDA runtime call failed                         */
-  PI_ERR_INDEX = 10      /* device: an active-list entry is outside [0, n)     */
+  PI_ERR_INDEX = 10,     /* device: an active-list entry is outside [0, n)     */
+  PI_ERR_RANGE = 11      /* device: a predictor partial sum exceeds the range
+                            of the fixed-point exchange (|value| >= 2^23)      */
 } pi_status;
 
 typedef enum { PI_F16 = 0, PI_BF16 = 1 } pi_dtype;
@@ -172,7 +174,9 @@ pi_status pi_sparse_ffn(const pi_ffn_desc* desc, const pi_layer_weights* w,
 
 /* Dense FFN over all n neurons, the comparison point of the sparse path:
  *     y[t] = b2 + sum_i ReLU(W1_i . x[t] + b1_i) W2_i   (gated as above).
- * batch <= 32. */
+ * batch <= 32.  batch > 1 with d % 128 == 0 reads every row once for all
+ * tokens on the tensor cores (the batched sparse path over all n neurons);
+ * otherwise one persistent CUDA-core launch per token. */
 pi_status pi_dense_ffn(const pi_ffn_desc* desc, const pi_layer_weights* w,
                        const float* x, int32_t batch, float* y, void* ws,
                        size_t ws_bytes, pi_stream stream);
@@ -193,6 +197,30 @@ pi_status pi_layer_decode(const pi_ffn_desc* desc, const pi_layer_weights* w,
                           const float* residual, int32_t* idx_out,
                           int32_t* cnt_out, int32_t* dev_status, void* ws,
                           size_t ws_bytes, pi_stream stream);
+
+/* Batch-1 decode through a sequence of J layer steps in one persistent
+ * launch: the same per-layer computation as pi_layer_decode ("Online
+ * Section", "Neuron Conscious Operator"), with each step's weights that do
+ * not depend on its input (hot rows, predictor rows) fetched while the
+ * previous step finishes; a step's input is read only after the previous
+ * step is complete.
+ *   descs / layers: host arrays of R (1 <= R <= 128) layers with one shape
+ *     (d, n, r, dtype, gated, layout equal; hot_prefix may differ);
+ *     step j uses layer j % R.
+ *   chain = 1: a residual stack, x_0 = x [d], x_{j+1} = x_j + FFN_j(x_j),
+ *     y[j] = x_{j+1};  chain = 0: independent steps, x [J][d] (one input
+ *     per step), y[j] = FFN_j(x[j]).  y: [J][d] fp32.
+ *   cnt_out: NULL or [J], active neurons of each step; mask_out: NULL or
+ *     [J][n] bytes, 1 where the neuron was predicted active.
+ *   ws: pi_workspace_size(&descs[0], 1) bytes.  Needs d / 8 <= 8 x the
+ *   number of SMs.  Device-side errors go to *dev_status as in
+ *   pi_layer_decode.  The paper has no counterpart: it decodes one layer
+ *   call at a time. */
+pi_status pi_decode_layers(const pi_ffn_desc* descs, const pi_layer_weights* layers,
+                           int32_t R, int32_t J, const float* x, int32_t chain,
+                           float* y, int32_t* cnt_out, uint8_t* mask_out,
+                           int32_t* dev_status, void* ws, size_t ws_bytes,
+                           pi_stream stream);
 
 /* pi_layer_decode for batch 1 without a caller-provided workspace.  The
  * paper has no counterpart to this call; it exists for callers that cannot

@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for s in range(11):
+    for s in range(12):
         assert len(pi.status_string(s)) >= 2
     assert pi.status_string(0) == "ok"
     assert "unknown" in pi.status_string(99)
@@ -114,6 +114,34 @@ def test_host_validation_before_launch(lib):
     assert L.pi_pack_weights(by(d), P + 2, P, P, None) == pi.PI_ERR_ALIGN
     assert L.pi_selftest_wait_timeout(P, P, 64, 1000000, None) == pi.PI_ERR_WORKSPACE
     assert L.pi_selftest_wait_timeout(P, P, 4096, 10, None) == pi.PI_ERR_SHAPE
+
+
+def test_decode_layers_host_validation(lib):
+    P = 1 << 40
+    d = pi.make_desc(1024, 4096, 64, "f16", hot_prefix=90)
+    w = pi.make_weights(P, P, P, P, P, None)
+    wsb = pi.pi_workspace_size(d, 1)
+
+    def f(*args):
+        return pi.pi_decode_layers(*args, stream=0)  # the legacy stream: no torch.cuda here
+    # layer count, step count, chain flag
+    assert f([], [], 1, P, 1, P, None, None, P, P, wsb) == pi.PI_ERR_SHAPE
+    assert f([d] * 129, [w] * 129, 1, P, 1, P, None, None, P, P, wsb) == pi.PI_ERR_SHAPE
+    assert f([d], [w], 0, P, 1, P, None, None, P, P, wsb) == pi.PI_ERR_SHAPE
+    assert f([d], [w], 4, P, 2, P, None, None, P, P, wsb) == pi.PI_ERR_SHAPE
+    # layers of different shapes; hot prefixes may differ
+    e = pi.make_desc(1024, 4096, 128, "f16")
+    assert f([d, e], [w, w], 2, P, 1, P, None, None, P, P, wsb) == pi.PI_ERR_SHAPE
+    g = pi.make_desc(1024, 4096, 64, "f16", gated=True)
+    assert f([d, g], [w, w], 2, P, 1, P, None, None, P, P, wsb) == pi.PI_ERR_SHAPE
+    # predictor weights required; NULL / misaligned buffers; small workspace
+    wn = pi.make_weights(None, P, P, P, P, None)
+    assert f([d], [wn], 1, P, 1, P, None, None, P, P, wsb) == pi.PI_ERR_NULL
+    assert f([d], [w], 1, None, 1, P, None, None, P, P, wsb) == pi.PI_ERR_NULL
+    assert f([d], [w], 1, P, 1, P, None, None, None, P, wsb) == pi.PI_ERR_NULL
+    assert f([d], [w], 1, P + 4, 1, P, None, None, P, P, wsb) == pi.PI_ERR_ALIGN
+    assert f([d], [w], 1, P, 1, P, P + 4, None, P, P, wsb) == pi.PI_ERR_ALIGN
+    assert f([d], [w], 1, P, 1, P, None, None, P, P, wsb - 256) == pi.PI_ERR_WORKSPACE
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):

@@ -134,3 +134,36 @@ def test_batched_empty_union():
     y, idxs, st = decode_batch(D, x)
     assert st == 0 and all(len(i) == 0 for i in idxs)
     np.testing.assert_array_equal(y, np.broadcast_to(L.b2, y.shape))
+
+
+@pytest.mark.parametrize("batch", [2, 16, 32])
+def test_dense_batched(batch):
+    D = dev_layer("ragged", lambda: synth.make_layer(256, 1001, 24, "f16", alpha=0.9,
+                                                      density=0.15, seed=61))
+    L = D.L
+    x = synth.gen_x(64, batch, batch, L.d)
+    y = torch.empty((batch, L.d), device=DEV)
+    pi.check(pi.pi_dense_ffn(D.desc, D.w, up(x, DEV), batch, y, D.workspace(batch)))
+    torch.cuda.synchronize()
+    yh = y.cpu().numpy()
+    for t in range(batch):
+        yd = oracle.dense_ffn(L, x[t])
+        assert float(np.abs(yh[t] - yd).max()) / float(np.abs(yd).max()) <= Y_TOL
+
+
+def test_dense_batched_gated_full_size():
+    D = dev_layer("llama", lambda: synth.make_layer(4096, 11008, 256, "bf16", gated=True,
+                                                     alpha=1.0, density=0.10, seed=3))
+    x = synth.gen_x(65, 0, 4, D.L.d)
+    for packed in (False, True):
+        D.set_packed(packed)
+        try:
+            y = torch.empty((4, D.L.d), device=DEV)
+            pi.check(pi.pi_dense_ffn(D.desc, D.w, up(x, DEV), 4, y, D.workspace(4)))
+            torch.cuda.synchronize()
+        finally:
+            D.set_packed(False)
+        yh = y.cpu().numpy()
+        for t in (0, 3):
+            yd = oracle.dense_ffn(D.L, x[t])
+            assert float(np.abs(yh[t] - yd).max()) / float(np.abs(yd).max()) <= Y_TOL
