@@ -129,73 +129,49 @@ __device__ __forceinline__ void prefetch_neuron(const FfnArgs& a, int i) {
 }
 
 // ------------------------------------------------------------ predictor (fused)
-// Logits of this block's own neurons i = c + j P (j < rows); flag[j] =
-// (logit > 0).  A row is rc = r / 8 sixteen-byte pieces.
-//   Rows staged in shared memory: four lanes per row, eight rows per warp at
-//   a time, each lane summing its pieces l, l + 4, ...
-//   Rows read through L2: RC lanes (the power of two >= rc) take one row, so
-//   one warp load covers 32 / RC rows, and each lane keeps up to NB row
-//   loads in flight before the first use.
-// A row's lane sums meet in a fixed shuffle tree.
-template <int DT, int NB = 12>
+// Logits of this block's own neurons i = c + j P (j < rows), four lanes per
+// row, eight rows per warp at a time; flag[j] = (logit > 0).  A lane takes
+// the row's sixteen-byte pieces l, l + 4, ... in batches of four loads issued
+// before their first use (rows staged in shared memory, or read via L2).
+template <int DT>
 __device__ void own_logits(const FfnArgs& a, const unsigned char* As, const float* b1s,
                            const float* us, unsigned char* flag, int rows) {
   const int rc = a.r >> 3;
-  if (a.a_in_smem) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, l = lane & 3;
-    for (int base = warp * 8; base < rows; base += kWarps * 8) {
-      const int j = base + g;
-      float acc = 0.f;
-      if (j < rows) {
-        for (int q = l; q < rc; q += 4) {
-          float f[8], u[8];
-          unpack8<DT>(*reinterpret_cast<const uint4*>(As + (size_t)j * a.a_stride + 16 * q), f);
-          load8(us + 8 * q, u);
-          acc += dot8(f, u);
-        }
-      }
-      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-      if (j < rows && l == 0) flag[j] = (acc + b1s[j] > 0.f) ? 1 : 0;
-    }
-    return;
-  }
-  int RC = 1;
-  while (RC < rc) RC <<= 1;
-  const int per = 32 / RC;
   const int c = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int sub = lane / RC, l = lane - sub * RC;
-  const bool lane_ok = l < rc;
-  float u[8];
-  if (lane_ok) {
-    load8(us + 8 * l, u);
-  } else {
+  const int g = lane >> 2, l = lane & 3;
+  constexpr int QT = 4;
+  for (int base = warp * 8; base < rows; base += kWarps * 8) {
+    const int j = base + g;
+    float acc = 0.f;
+    if (j < rows) {
+      for (int q0 = l; q0 < rc; q0 += 4 * QT) {
+        uint4 v[QT];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) u[e] = 0.f;
-  }
-  const int stride = kWarps * per;  // rows of one block-wide load round
-  for (int b0 = warp * per; b0 < rows; b0 += NB * stride) {  // warp-uniform
-    uint4 v[NB];
+        for (int t = 0; t < QT; ++t) {
+          const int q = q0 + 4 * t;
+          if (q < rc) {
+            if (a.a_in_smem)
+              v[t] = *reinterpret_cast<const uint4*>(As + (size_t)j * a.a_stride + 16 * q);
+            else
+              v[t] = ld_nc(a.A + ((size_t)c + (size_t)j * a.P) * a.r + 8 * q);
+          }
+        }
 #pragma unroll
-    for (int t = 0; t < NB; ++t) {
-      const int j = b0 + sub + t * stride;
-      if (lane_ok && j < rows) v[t] = ld_nc(a.A + ((size_t)c + (size_t)j * a.P) * a.r + 8 * l);
-    }
-#pragma unroll
-    for (int t = 0; t < NB; ++t) {
-      const int j = b0 + sub + t * stride;
-      if (b0 + t * stride >= rows) break;  // warp-uniform: no row of this round left
-      float acc = 0.f;
-      if (lane_ok && j < rows) {
-        float f[8];
-        unpack8<DT>(v[t], f);
-        acc = dot8(f, u);
+        for (int t = 0; t < QT; ++t) {
+          const int q = q0 + 4 * t;
+          if (q < rc) {
+            float f[8], u[8];
+            unpack8<DT>(v[t], f);
+            load8(us + 8 * q, u);
+            acc += dot8(f, u);
+          }
+        }
       }
-      for (int o = RC >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if (l == 0 && j < rows) flag[j] = (acc + b1s[j] > 0.f) ? 1 : 0;
     }
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    if (j < rows && l == 0) flag[j] = (acc + b1s[j] > 0.f) ? 1 : 0;
   }
 }
 

@@ -26,6 +26,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct WsLayout {
   size_t ctrl, upart, loc_tot, mask, part, u, logits, total;
   size_t uacc;  // sequence kernel: 2 x r fixed-point accumulators, one 128-byte line each
+  size_t glist, gcnt;  // sequence kernel: published cold entries and counts
   // batched path (batch > 1)
   size_t bidx, bcnt, uidx, ucnt, tmask, xhi, xlo, hhi, hlo, bpart;
   int bp, hs;
@@ -51,6 +52,8 @@ WsLayout ws_layout(const pi_ffn_desc& D, int batch) {
   L.u = take(sizeof(float) * (size_t)batch * D.r);
   L.logits = take(sizeof(float) * (size_t)batch * D.n);
   L.uacc = take(2 * 128 * (size_t)D.r);
+  L.glist = take(8 * ((size_t)D.n + kPMax));
+  L.gcnt = take(sizeof(int) * kPMax);
   L.bp = batch_pad(batch);
   L.hs = h_stride(D.n);
   if (batch > 1) {
@@ -734,6 +737,7 @@ pi_status pi_decode_layers(const pi_ffn_desc* descs, const pi_layer_weights* lay
   if (s != PI_OK) return s;
   const int P = di.sms < kPMax ? di.sms : kPMax;
   if ((D.d / 8 + P - 1) / P > kSeqMaxQ) return PI_ERR_SHAPE;  // own columns per block
+  if ((D.n + P - 1) / P > 32 * 256) return PI_ERR_SHAPE;      // own neurons per block
   D.hot_prefix = hot_max;
   const bool wide = (D.d / 8) > kThreads;
   SeqFn fn = pick_seq(D.dtype, D.gated, wide);
@@ -760,6 +764,11 @@ pi_status pi_decode_layers(const pi_ffn_desc* descs, const pi_layer_weights* lay
   sa.uacc = reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) + L.uacc);
   const int qmax = (D.d / 8 + P - 1) / P;
   sa.bm_smem = (a.nh < a.ns - 1 && D.r * qmax * 16 <= a.slot_bytes) ? 1 : 0;
+  sa.glist = reinterpret_cast<int2*>(static_cast<char*>(ws) + L.glist);
+  sa.gcnt = reinterpret_cast<int*>(static_cast<char*>(ws) + L.gcnt);
+  sa.balance = 0;  // measured: no gain on the 48-layer stack (its extra wait costs the tail)
+  if (const char* e = std::getenv("PI_SEQ_BALANCE")) sa.balance = std::atoi(e) != 0;
+
   for (int l = 0; l < R; ++l) {
     const pi_layer_weights& w = layers[l];
     SeqLayer& e = sa.L[l];

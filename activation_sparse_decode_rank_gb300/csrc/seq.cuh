@@ -27,6 +27,9 @@
 //      predictor rows towards L2 / shared memory) are requested, so that
 //      their transfer overlaps this job's tail;
 //   -- wait 2 -- (partial rows written)
+// With balancing on (large layers), the blocks publish their cold active
+// neurons after the lists are built and, after one more grid-wide wait, each
+// takes an equal share of them by global rank.
 // A job's x is read only after the previous job is complete: jobs never
 // overlap in anything that depends on their inputs.
 #pragma once
@@ -58,6 +61,9 @@ struct SeqArgs {
   unsigned char* mask_out;  // [J][n] or NULL
   unsigned long long* uacc;  // [2][r] fixed-point u, 16 words (128 bytes) apart; zero at launch
   int bm_smem;            // stage the next job's own Bm columns in the last ring slot
+  int balance;            // spread the cold active neurons evenly (one more grid-wide wait)
+  int2* glist;            // [P][rows_max] published cold entries (neuron, b1 bits)
+  int* gcnt;              // [P] published cold counts
   SeqLayer L[kSeqMaxLayers];
 };
 
@@ -86,10 +92,10 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
   const int rows = (c < f.n) ? (f.n - 1 - c) / P + 1 : 0;  // own neurons c, c + P, ...
   const int q0 = (int)((long long)c * f.nch / P), q1 = (int)((long long)(c + 1) * f.nch / P);
   const int nq = q1 - q0;  // own 8-column chunks (<= kSeqMaxQ, checked by the host)
-  const int rc = f.r >> 3;
 
   unsigned char* bms = slots + (size_t)(f.ns - 1) * f.slot_bytes;  // staged Bm columns
   FfnArgs a = f;  // the current job's weights
+  const int rc = f.r >> 3;
   int nh_c = 0;   // own hot neurons whose rows went to slots for the current job
 
   // Requests the weights of job j that do not depend on its x.  No copy may
@@ -120,27 +126,27 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
     }
     armed = true;
     if (compute) {
-      // the small copies the next phases wait for go out first: own Bm
-      // columns ([k][q], 16 bytes each, into the last ring slot, a cold one),
-      // biases, staged predictor rows; then the predictor rows towards L2
+      // the own hot neurons beyond the slots and (unless staged) the own
+      // predictor rows towards L2; staged predictor rows, biases and own Bm
+      // columns ([k][q], 16 bytes each, in the last ring slot, a cold one)
+      for (int k = nh_c + tid; k < hot_own; k += kThreads) prefetch_neuron<GATED>(a, c + k * P);
+      if (f.a_in_smem) {
+        for (int e = tid; e < rows * rc; e += kThreads) {
+          const int jj = e / rc, q = e - jj * rc;
+          cp_async16(As + (size_t)jj * f.a_stride + 16 * q,
+                     a.A + ((size_t)c + (size_t)jj * P) * f.r + 8 * q);
+        }
+      } else {
+        for (int jj = tid; jj < rows; jj += kThreads)
+          prefetch_l2(a.A + ((size_t)c + (size_t)jj * P) * f.r, (size_t)f.r * 2);
+      }
       if (sa.bm_smem)
         for (int e = tid; e < f.r * nq; e += kThreads) {
           const int k = e / nq, q = e - k * nq;
           cp_async16(bms + (size_t)e * 16, a.Bm + (size_t)k * f.d + 8 * (q0 + q));
         }
       for (int jj = tid; jj < rows; jj += kThreads) cp_async4(b1s + jj, a.b1 + c + (size_t)jj * P);
-      if (f.a_in_smem)
-        for (int e = tid; e < rows * rc; e += kThreads) {
-          const int jj = e / rc, q = e - jj * rc;
-          cp_async16(As + (size_t)jj * f.a_stride + 16 * q,
-                     a.A + ((size_t)c + (size_t)jj * P) * f.r + 8 * q);
-        }
       cp_async_commit();
-      if (!f.a_in_smem)
-        for (int jj = tid; jj < rows; jj += kThreads)
-          prefetch_l2(a.A + ((size_t)c + (size_t)jj * P) * f.r, (size_t)f.r * 2);
-      // the own hot neurons beyond the slots, towards L2
-      for (int k = nh_c + tid; k < hot_own; k += kThreads) prefetch_neuron<GATED>(a, c + k * P);
     }
   };
   // On a failed grid-wide wait: let this block's own copies land, then leave.
@@ -213,32 +219,112 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
     }
     cp_async_wait_all();
     __syncthreads();
-    if (compute) own_logits<DT, 6>(a, As, b1s, us, flag, rows);
+    if (compute) own_logits<DT>(a, As, b1s, us, flag, rows);
     __syncthreads();
-    if (warp == 0) {
+    {
+      // ordered list of the own active neurons, all compute warps: warp w
+      // takes 32-row chunks w, w + 16, ...; chunk counts, their exclusive
+      // prefix (warp 0), then every warp writes its entries.  The hot ones
+      // whose rows sit in slots (row < nh_c <= 16, chunk 0) come first.
       unsigned char* mrow = sa.mask_out ? sa.mask_out + (size_t)j * f.n : nullptr;
-      int cnt = 0, nhot = 0;
-      for (int base = 0; base < rows; base += 32) {
-        const int jj = base + lane;
-        const bool fl = (jj < rows) && flag[jj];
-        const unsigned bal = __ballot_sync(0xffffffffu, fl);
-        const int pos = cnt + __popc(bal & ((1u << lane) - 1u));
-        if (fl) {
-          lst[pos] = c + jj * P;
-          lb[pos] = b1s[jj];
+      int* ccnt = reinterpret_cast<int*>(red);  // chunk counts, then offsets
+      const int nck = (rows + 31) >> 5;         // <= 256 (checked by the host)
+      if (compute)
+        for (int ch = warp; ch < nck; ch += kWarps) {
+          const int jj = ch * 32 + lane;
+          const unsigned bal = __ballot_sync(0xffffffffu, jj < rows && flag[jj]);
+          if (lane == 0) ccnt[ch] = __popc(bal);
         }
-        if (mrow && jj < rows) mrow[(size_t)c + (size_t)jj * P] = fl ? 1 : 0;
-        cnt += __popc(bal);
-        nhot += __popc(__ballot_sync(0xffffffffu, fl && jj < nh_c));
+      __syncthreads();
+      if (warp == 0) {
+        int run = 0;
+        for (int b0 = 0; b0 < nck; b0 += 32) {
+          const int b = b0 + lane;
+          const int v0 = (b < nck) ? ccnt[b] : 0;
+          int v = v0;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += t;
+          }
+          if (b < nck) ccnt[b] = run + v - v0;
+          run += __shfl_sync(0xffffffffu, v, 31);
+        }
+        if (lane == 0) {
+          s_m = run;
+          s_mh = 0;  // set below from chunk 0, if the block has rows
+          __stcg(f.loc_tot + c, run);
+        }
       }
-      if (lane == 0) {
-        s_m = cnt;
-        s_mh = nhot;
-        __stcg(f.loc_tot + c, cnt);
-      }
+      __syncthreads();
+      if (compute)
+        for (int ch = warp; ch < nck; ch += kWarps) {
+          const int jj = ch * 32 + lane;
+          const bool fl = jj < rows && flag[jj];
+          const unsigned bal = __ballot_sync(0xffffffffu, fl);
+          if (fl) {
+            const int pos = ccnt[ch] + __popc(bal & ((1u << lane) - 1u));
+            lst[pos] = c + jj * P;
+            lb[pos] = b1s[jj];
+          }
+          if (mrow && jj < rows) mrow[(size_t)c + (size_t)jj * P] = fl ? 1 : 0;
+          if (ch == 0) {
+            const unsigned hb = __ballot_sync(0xffffffffu, fl && jj < nh_c);
+            if (lane == 0) s_mh = __popc(hb);
+          }
+        }
     }
     __syncthreads();
-    const int m = s_m, mh = s_mh;
+    int m = s_m;
+    const int mh = s_mh;
+    if (sa.balance) {
+      // Cold entries (those without a slot) are spread over the blocks by
+      // their rank in the concatenation of all blocks' lists: block c takes
+      // ranks c, c + P, ...  The split depends only on the lists, so the
+      // per-block sums keep a fixed order.
+      int2* gl = sa.glist + (size_t)c * f.rows_max;
+      for (int e = tid; e < m - mh; e += kBlock)
+        gl[e] = make_int2(lst[mh + e], __float_as_int(lb[mh + e]));
+      if (tid == 0) __stcg(sa.gcnt + c, m - mh);
+      ++nbar;
+      if (!grid_sync(f.bar, s_base + nbar * P, f.status, f.limit_ns)) {
+        bail();
+        return;
+      }
+      int* pre = reinterpret_cast<int*>(red);  // [P + 1] exclusive prefix of the counts
+      if (warp == 0) {
+        int run = 0;
+        for (int b0 = 0; b0 < P; b0 += 32) {
+          const int b = b0 + lane;
+          int v = (b < P) ? __ldcg(sa.gcnt + b) : 0;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += t;
+          }
+          if (b < P) pre[b + 1] = run + v;
+          run += __shfl_sync(0xffffffffu, v, 31);
+        }
+        if (lane == 0) pre[0] = 0;
+      }
+      __syncthreads();
+      const int C = pre[P];
+      const int mc = (C > c) ? (C - 1 - c) / P + 1 : 0;
+      for (int t = tid; t < mc; t += kBlock) {
+        const int k = c + t * P;
+        int lo = 0, hi = P;  // pre[lo] <= k < pre[hi]
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (pre[mid] <= k) lo = mid;
+          else hi = mid;
+        }
+        const int2 e = __ldcg(sa.glist + (size_t)lo * f.rows_max + (k - pre[lo]));
+        lst[mh + t] = e.x;
+        lb[mh + t] = __int_as_float(e.y);
+      }
+      __syncthreads();
+      m = mh + mc;
+    }
     float yacc[NCH][8];
 #pragma unroll
     for (int q = 0; q < NCH; ++q)

@@ -754,9 +754,11 @@ def main():
     ap.add_argument("--graph-len", type=int, default=2000)
     ap.add_argument("--e2e-steps", type=int, default=20000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--engine", default="call", choices=["call", "seq"],
-                    help="call: one pi_layer_decode launch per step; seq: pi_decode_layers, "
-                         "one persistent launch per graph-length chunk of steps")
+    ap.add_argument("--engine", default="auto", choices=["auto", "call", "seq"],
+                    help="call: one pi_layer_decode launch per step (per layer); seq: "
+                         "pi_decode_layers, one persistent launch per graph-length chunk of "
+                         "steps (per token for a stack); auto: seq for one layer, call for "
+                         "a stack (the faster of the two on each, as measured on GB300)")
     ap.add_argument("--sweep", action="store_true",
                     help="batched decode / density sweep (with --workload opt13b_ffn_batched_...)")
     args = ap.parse_args()
@@ -766,7 +768,10 @@ def main():
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
-    if workload_spec(args.workload).get("layers", 1) > 1:
+    stack = workload_spec(args.workload).get("layers", 1) > 1
+    if args.engine == "auto":
+        args.engine = "call" if stack else "seq"
+    if stack:
         return run_stack(args)
     return run_ours(args)
 

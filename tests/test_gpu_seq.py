@@ -66,15 +66,20 @@ def tiny_layers(R, seed=21, dtype="f16", gated=False, hot=90, packed=False):
     return out
 
 
-@pytest.mark.parametrize("packed", [False, True])
-def test_stack_chain_tiny(packed):
+@pytest.mark.parametrize("packed,balance", [(False, "0"), (True, "0"), (False, "1"), (True, "1")])
+def test_stack_chain_tiny(packed, balance, monkeypatch):
+    # balance = 1: the cold active neurons are spread over the blocks by
+    # global rank (one more grid-wide wait); the results obey the same rules
+    monkeypatch.setenv("PI_SEQ_BALANCE", balance)
     layers = tiny_layers(4, packed=packed)
     x = synth.gen_x(21, 0, 1, 1024)
     y, mask, cnt = run_seq(layers, 4, x, chain=True)
     assert check_steps(layers, 4, x, True, y, mask, cnt) <= 8
 
 
-def test_independent_steps_wrap_the_table():
+@pytest.mark.parametrize("balance", ["0", "1"])
+def test_independent_steps_wrap_the_table(balance, monkeypatch):
+    monkeypatch.setenv("PI_SEQ_BALANCE", balance)
     layers = tiny_layers(3, seed=22, hot=0)
     J = 7
     x = synth.gen_x(22, 0, J, 1024)
@@ -129,7 +134,9 @@ def test_opt67_shape_matches_layer_decode():
         assert float(np.abs(y1.cpu().numpy()[0] - y[j]).max()) <= 2 * Y_TOL * float(np.abs(yd).max())
 
 
-def test_opt30_shape_stack_three_layers():
+@pytest.mark.parametrize("balance", ["0", "1"])
+def test_opt30_shape_stack_three_layers(balance, monkeypatch):
+    monkeypatch.setenv("PI_SEQ_BALANCE", balance)
     d, n, r = 7168, 28672, 256
     seed = 4
     alpha, rho, cz, scale = synth.stack_plan(seed, 48, n)
