@@ -104,6 +104,127 @@ __device__ __forceinline__ void split16(float v, uint16_t* hi, uint16_t* lo) {
   }
 }
 
+// ---------------------------------------------------------------- batched predictor
+// Stage 1 split over the columns: block c of G owns the 8-column chunks
+// [c nch / G, (c+1) nch / G) and writes the partial u of every (token, k),
+// part[c][t][k]; thread k keeps the batch's sums in registers, x's columns
+// of the block are staged in shared memory.
+template <int DT, int TB>
+__global__ void __launch_bounds__(256) bpu_partial_kernel(const uint16_t* Bm, const float* x, int d,
+                                                          int r, int batch, int G, float* part) {
+  extern __shared__ __align__(16) float xs[];  // [batch][w]
+  const int c = blockIdx.x, tid = threadIdx.x, nch = d >> 3;
+  const int q0 = (int)((long long)c * nch / G), q1 = (int)((long long)(c + 1) * nch / G);
+  const int nq = q1 - q0, w = nq * 8;
+  for (int e = tid; e < batch * w; e += 256) {
+    const int t = e / w, j = e - t * w;
+    xs[e] = x[(size_t)t * d + 8 * q0 + j];
+  }
+  __syncthreads();
+  for (int k = tid; k < r; k += 256) {
+    float acc[TB];
+#pragma unroll
+    for (int t = 0; t < TB; ++t) acc[t] = 0.f;
+    const uint16_t* row = Bm + (size_t)k * d + 8 * q0;
+    for (int q = 0; q < nq; ++q) {
+      float f[8];
+      unpack8<DT>(ld_nc(row + 8 * q), f);
+#pragma unroll
+      for (int t = 0; t < TB; ++t) {
+        if (t < batch) {
+          float xv[8];
+          load8(xs + t * w + 8 * q, xv);
+          acc[t] += dot8(f, xv);
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < TB; ++t)
+      if (t < batch) part[((size_t)c * batch + t) * r + k] = acc[t];
+  }
+}
+
+// u[t][k] = sum_c part[c][t][k] (c ascending), then its high / low 16-bit
+// parts for the tensor cores ([bp][r]; zero rows for padded tokens).
+template <int DT>
+__global__ void __launch_bounds__(256) bpu_reduce_kernel(const float* part, int r, int batch, int bp,
+                                                         int G, uint16_t* uhi, uint16_t* ulo) {
+  const int e = blockIdx.x * 256 + threadIdx.x;  // t * r + k
+  if (e >= bp * r) return;
+  const int t = e / r, k = e - t * r;
+  float s = 0.f;
+  if (t < batch) {
+#pragma unroll 8
+    for (int c = 0; c < G; ++c) s += part[((size_t)c * batch + t) * r + k];
+  }
+  uint16_t hi, lo;
+  split16<DT>(s, &hi, &lo);
+  uhi[e] = hi;
+  ulo[e] = lo;
+}
+
+// logits[t][i] = A_i . u[t] + b1_i on the tensor cores: block = 64 neurons x
+// all tokens, K = r.  A rows (the B operand, one neuron per row) and u's
+// high / low parts (the A operand, one token per row) staged in shared
+// memory with 16-byte row padding; warp w takes neurons 8w .. 8w + 7.
+constexpr int kLT = 64;
+template <int DT, int MT>
+__global__ void __launch_bounds__(256) blogit_kernel(const uint16_t* A, const float* b1,
+                                                     const uint16_t* uhi, const uint16_t* ulo, int n,
+                                                     int r, int batch, int bp, float* logits) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rowb = 2 * r + 16;
+  unsigned char* As = smem;               // [kLT][rowb]
+  unsigned char* Us = smem + kLT * rowb;  // [2 bp][rowb]: high parts, then low parts
+  const int i0 = blockIdx.x * kLT;
+  const int tn = min(kLT, n - i0);
+  const int pcs = r >> 3;
+  for (int e = tid; e < kLT * pcs; e += 256) {
+    const int row = e / pcs, pc = e - row * pcs;
+    unsigned char* dst = As + (size_t)row * rowb + 16 * pc;
+    if (row < tn) cp_async16(dst, A + (size_t)(i0 + row) * r + 8 * pc);
+    else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  for (int e = tid; e < 2 * bp * pcs; e += 256) {
+    const int rw = e / pcs, pc = e - rw * pcs;
+    const int prt = rw / bp, t = rw - prt * bp;
+    cp_async16(Us + (size_t)rw * rowb + 16 * pc, (prt == 0 ? uhi : ulo) + (size_t)t * r + 8 * pc);
+  }
+  cp_async_commit();
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+  float acc[MT][4];
+#pragma unroll
+  for (int m = 0; m < MT; ++m)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[m][e] = 0.f;
+  for (int ks = 0; ks < (r >> 4); ++ks) {
+    uint32_t b[2];
+    ldsm_x2(b, As + (size_t)(warp * 8 + (lane & 7)) * rowb + (ks * 16 + 8 * ((lane >> 3) & 1)) * 2);
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      uint32_t ah[4], al[4];
+      const int rr = m * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+      const int cb = (ks * 16 + 8 * (lane >> 4)) * 2;
+      ldsm_x4(ah, Us + (size_t)rr * rowb + cb);
+      ldsm_x4(al, Us + (size_t)(bp + rr) * rowb + cb);
+      mma16816<DT>(acc[m], ah, b);
+      mma16816<DT>(acc[m], al, b);
+    }
+  }
+  const int g = lane >> 2, tq = lane & 3;
+#pragma unroll
+  for (int m = 0; m < MT; ++m)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int t = m * 16 + g + 8 * (e >> 1);
+      const int col = warp * 8 + 2 * tq + (e & 1);
+      if (t < batch && col < tn)
+        logits[(size_t)t * n + i0 + col] = acc[m][e] + __ldg(b1 + i0 + col);
+    }
+}
+
 // ---------------------------------------------------------------- phase 0
 // xhi/xlo[t][j] = split(x[t][j]) for t < batch, 0 for padded rows.
 template <int DT>

@@ -854,6 +854,113 @@ __global__ void __launch_bounds__(1024) union_kernel(const float* logits, int n,
   if (threadIdx.x == 0) *ucnt = out;
 }
 
+// ------------------------------------------------------------ grid-wide compaction
+// The same lists as compact_kernel / union_kernel, computed by the whole
+// grid: blocks of kCB neurons; series t < batch are the tokens' lists,
+// series 32 the union.
+//   pass 1: each block's count per series -> scr[s][b];
+//   pass 2 (one block): exclusive prefix of every series over the blocks,
+//           in place, totals -> scr[33 nb + s];
+//   pass 3: each block writes its entries at its offsets (ascending order),
+//           the last block the counts.
+constexpr int kCB = 256;
+constexpr int kCSeries = 33;
+
+__device__ __forceinline__ uint32_t token_mask(const float* logits, int n, int batch, int i) {
+  uint32_t m = 0u;
+  if (i < n)
+    for (int t = 0; t < batch; ++t) m |= (logits[(size_t)t * n + i] > 0.f ? 1u : 0u) << t;
+  return m;
+}
+
+__global__ void __launch_bounds__(kCB) cu_count_kernel(const float* logits, int n, int batch,
+                                                       int want_union, int* scr, int nb) {
+  __shared__ int wc[kCSeries][kCB / 32];
+  const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t m = token_mask(logits, n, batch, b * kCB + tid);
+  for (int t = 0; t < batch; ++t) {
+    const unsigned bal = __ballot_sync(0xffffffffu, (m >> t) & 1u);
+    if (lane == 0) wc[t][warp] = __popc(bal);
+  }
+  const unsigned bu = __ballot_sync(0xffffffffu, m != 0u);
+  if (lane == 0) wc[32][warp] = __popc(bu);
+  __syncthreads();
+  if (tid < kCSeries && (tid < batch || (tid == 32 && want_union))) {
+    int sum = 0;
+    for (int w = 0; w < kCB / 32; ++w) sum += wc[tid][w];
+    scr[(size_t)tid * nb + b] = sum;
+  }
+}
+
+__global__ void __launch_bounds__(1024) cu_scan_kernel(int* scr, int nb, int batch, int want_union) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int s = warp; s < kCSeries; s += 32) {
+    if (!(s < batch || (s == 32 && want_union))) continue;
+    int* row = scr + (size_t)s * nb;
+    int run = 0;
+    for (int b0 = 0; b0 < nb; b0 += 32) {
+      const int b = b0 + lane;
+      const int v0 = (b < nb) ? row[b] : 0;
+      int v = v0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+      }
+      if (b < nb) row[b] = run + v - v0;
+      run += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) scr[(size_t)kCSeries * nb + s] = run;
+  }
+}
+
+__global__ void __launch_bounds__(kCB) cu_write_kernel(const float* logits, int n, int batch,
+                                                       const int* scr, int nb, int* idx, int* cnt,
+                                                       int cap, int* uidx, int* ucnt,
+                                                       uint32_t* tmask, int* status) {
+  __shared__ int wc[kCSeries][kCB / 32];
+  __shared__ unsigned wb[kCSeries][kCB / 32];
+  const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int i = b * kCB + tid;
+  const uint32_t m = token_mask(logits, n, batch, i);
+  const bool want_union = uidx != nullptr;
+  for (int t = 0; t < batch; ++t) {
+    const unsigned bal = __ballot_sync(0xffffffffu, (m >> t) & 1u);
+    if (lane == 0) wb[t][warp] = bal;
+  }
+  const unsigned bu = __ballot_sync(0xffffffffu, m != 0u);
+  if (lane == 0) wb[32][warp] = bu;
+  __syncthreads();
+  if (tid < kCSeries) {  // exclusive offsets of the warps, after the blocks before this one
+    int run = (tid < batch || (tid == 32 && want_union)) ? scr[(size_t)tid * nb + b] : 0;
+    for (int w = 0; w < kCB / 32; ++w) {
+      wc[tid][w] = run;
+      run += __popc(wb[tid][w]);
+    }
+  }
+  __syncthreads();
+  const unsigned lt = (1u << lane) - 1u;
+  for (int t = 0; t < batch; ++t) {
+    if ((m >> t) & 1u) {
+      const int pos = wc[t][warp] + __popc(wb[t][warp] & lt);
+      if (pos < cap) idx[(size_t)t * cap + pos] = i;
+    }
+  }
+  if (want_union && m != 0u) {
+    const int pos = wc[32][warp] + __popc(bu & lt);
+    uidx[pos] = i;
+    tmask[pos] = m;
+  }
+  if (b == nb - 1) {
+    if (tid < batch) {
+      const int tot = scr[(size_t)kCSeries * nb + tid];
+      cnt[tid] = tot;
+      if (tot > cap) set_status(status, PI_ERR_CAPACITY);
+    }
+    if (tid == 32 && want_union) *ucnt = scr[(size_t)kCSeries * nb + 32];
+  }
+}
+
 // Failure-path diagnostic: one grid-wide wait whose last arrival never
 // comes (expected = grid + 1), so every block gives up after limit_ns.
 __global__ void wait_timeout_kernel(unsigned long long* bar, int* status,

@@ -27,12 +27,19 @@ struct WsLayout {
   size_t ctrl, upart, loc_tot, mask, part, u, logits, total;
   size_t uacc;  // sequence kernel: 2 x r fixed-point accumulators, one 128-byte line each
   size_t glist, gcnt;  // sequence kernel: published cold entries and counts
+  size_t cscr;         // grid-wide compaction counts (the last region: pi_compact finds it at
+                       // the end of the workspace)
   // batched path (batch > 1)
-  size_t bidx, bcnt, uidx, ucnt, tmask, xhi, xlo, hhi, hlo, bpart;
+  size_t bidx, bcnt, uidx, ucnt, tmask, xhi, xlo, hhi, hlo, bpart, ppart, uhi, ulo;
   int bp, hs;
 };
 
 int batch_pad(int batch) { return batch <= 16 ? 16 : 32; }
+// counts of the grid-wide compaction: [kCSeries][blocks] + totals
+size_t compact_scratch_bytes(int n) {
+  const size_t nb = ((size_t)n + kCB - 1) / kCB;
+  return round_up(sizeof(int) * (kCSeries * nb + kCSeries), 256);
+}
 int h_stride(int n) { return (int)round_up((size_t)n + kBN2, 64); }
 
 WsLayout ws_layout(const pi_ffn_desc& D, int batch) {
@@ -67,7 +74,11 @@ WsLayout ws_layout(const pi_ffn_desc& D, int batch) {
     L.hhi = take(2 * (size_t)L.bp * L.hs);
     L.hlo = take(2 * (size_t)L.bp * L.hs);
     L.bpart = take(sizeof(float) * (size_t)kGroups2 * L.bp * D.d);
+    L.ppart = take(sizeof(float) * (size_t)kPMax * batch * D.r);  // predictor partials [G][batch][r]
+    L.uhi = take(2 * (size_t)L.bp * D.r);
+    L.ulo = take(2 * (size_t)L.bp * D.r);
   }
+  L.cscr = take(compact_scratch_bytes(D.n));
   L.total = off;
   return L;
 }
@@ -433,6 +444,7 @@ WsLayout static_layout(const pi_ffn_desc& D, int P) {
   L.mask = take((size_t)D.n);
   L.part = take(sizeof(float) * (size_t)P * D.d);
   L.u = L.logits = 0;
+  L.cscr = take(compact_scratch_bytes(D.n));
   L.total = off;
   return L;
 }
@@ -527,6 +539,47 @@ pi_status pi_predict(const pi_ffn_desc* desc, const void* A, const void* Bm, con
   if (ws_bytes < L.total) return PI_ERR_WORKSPACE;
   const pi_ffn_desc& D = *desc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (batch > 1 && D.r % 16 == 0) {
+    // column-split stage 1 + fixed-order reduction, stage 2 on the tensor cores
+    DevInfo di;
+    pi_status s = dev_info(&di);
+    if (s != PI_OK) return s;
+    char* b = static_cast<char*>(ws);
+    float* part = reinterpret_cast<float*>(b + L.ppart);
+    uint16_t* uhi = reinterpret_cast<uint16_t*>(b + L.uhi);
+    uint16_t* ulo = reinterpret_cast<uint16_t*>(b + L.ulo);
+    const int nch = D.d / 8;
+    const int G = nch < di.sms ? nch : (di.sms < kPMax ? di.sms : kPMax);
+    const int wmax = 8 * ((nch + G - 1) / G);
+    const size_t smem1 = sizeof(float) * (size_t)batch * wmax;
+    const bool bf = D.dtype == PI_BF16;
+    const uint16_t* Bh = static_cast<const uint16_t*>(Bm);
+    const bool tb8 = batch <= 8;
+    if (!bf) {
+      if (tb8) bpu_partial_kernel<0, 8><<<G, 256, smem1, st>>>(Bh, x, D.d, D.r, batch, G, part);
+      else bpu_partial_kernel<0, 32><<<G, 256, smem1, st>>>(Bh, x, D.d, D.r, batch, G, part);
+    } else {
+      if (tb8) bpu_partial_kernel<1, 8><<<G, 256, smem1, st>>>(Bh, x, D.d, D.r, batch, G, part);
+      else bpu_partial_kernel<1, 32><<<G, 256, smem1, st>>>(Bh, x, D.d, D.r, batch, G, part);
+    }
+    if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
+    const int bp = L.bp;
+    const unsigned gr = (unsigned)((bp * D.r + 255) / 256);
+    if (!bf) bpu_reduce_kernel<0><<<gr, 256, 0, st>>>(part, D.r, batch, bp, G, uhi, ulo);
+    else bpu_reduce_kernel<1><<<gr, 256, 0, st>>>(part, D.r, batch, bp, G, uhi, ulo);
+    if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
+    const int smem2 = (kLT + 2 * bp) * (2 * D.r + 16);
+    using LFn = void (*)(const uint16_t*, const float*, const uint16_t*, const uint16_t*, int, int,
+                         int, int, float*);
+    LFn fl = bf ? (bp == 32 ? blogit_kernel<1, 2> : blogit_kernel<1, 1>)
+                : (bp == 32 ? blogit_kernel<0, 2> : blogit_kernel<0, 1>);
+    s = ensure_smem(reinterpret_cast<const void*>(fl), smem2);
+    if (s != PI_OK) return s;
+    fl<<<(unsigned)((D.n + kLT - 1) / kLT), 256, smem2, st>>>(
+        static_cast<const uint16_t*>(A), b1, uhi, ulo, D.n, D.r, batch, bp, logits);
+    if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
+    return PI_OK;
+  }
   float* u = reinterpret_cast<float*>(static_cast<char*>(ws) + L.u);
   const uint16_t* Bh = static_cast<const uint16_t*>(Bm);
   const uint16_t* Ah = static_cast<const uint16_t*>(A);
@@ -560,8 +613,6 @@ pi_status pi_predict(const pi_ffn_desc* desc, const void* A, const void* Bm, con
 pi_status pi_compact(const float* logits, int32_t n, int32_t batch, int32_t* idx, int32_t* cnt,
                      int32_t cap, int32_t* union_idx, int32_t* union_cnt, uint32_t* tok_mask,
                      int32_t* dev_status, void* ws, size_t ws_bytes, pi_stream stream) {
-  (void)ws;
-  (void)ws_bytes;
   if (n < 1 || n > (1 << 24) || batch < 1 || batch > kMaxBatch || cap < 0) return PI_ERR_SHAPE;
   if (!logits || !idx || !cnt) return PI_ERR_NULL;
   if (cap < n && !dev_status) return PI_ERR_NULL;
@@ -570,6 +621,20 @@ pi_status pi_compact(const float* logits, int32_t n, int32_t batch, int32_t* idx
   for (const void* p : ps)
     if (p && !aligned16(p)) return PI_ERR_ALIGN;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t need = compact_scratch_bytes(n);
+  if (ws && ws_bytes >= need) {
+    // grid-wide: counts in the workspace's last region (see ws_layout)
+    int* scr = reinterpret_cast<int*>(static_cast<char*>(ws) + ((ws_bytes - need) & ~(size_t)15));
+    const int nb = (n + kCB - 1) / kCB;
+    const int wu = union_idx ? 1 : 0;
+    cu_count_kernel<<<nb, kCB, 0, st>>>(logits, n, batch, wu, scr, nb);
+    cu_scan_kernel<<<1, 1024, 0, st>>>(scr, nb, batch, wu);
+    cu_write_kernel<<<nb, kCB, 0, st>>>(logits, n, batch, scr, nb, idx, cnt, cap, union_idx,
+                                        union_cnt, tok_mask, dev_status);
+    if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
+    return PI_OK;
+  }
+  // without a workspace: one block per token, one block for the union
   compact_kernel<<<batch, 1024, 0, st>>>(logits, n, idx, cnt, cap, dev_status);
   if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
   if (union_idx) {

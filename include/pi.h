@@ -140,7 +140,11 @@ pi_status pi_predict(const pi_ffn_desc* desc, const void* A, const void* Bm,
  *     union_idx[0 .. *union_cnt) = ascending { i : some token active }
  *     tok_mask[k] bit t set iff token t is active at neuron union_idx[k]
  * (capacity n for both; batch <= 32).  dev_status may be NULL only when no
- * capacity error can occur (cap >= n). */
+ * capacity error can occur (cap >= n).  ws: with a workspace of
+ * pi_workspace_size bytes (any descriptor with this n) the compaction runs
+ * over the whole grid, using the workspace's last region for its counts;
+ * with ws == NULL (or too small) it runs one block per token and one for
+ * the union (slower for large batches; same results). */
 pi_status pi_compact(const float* logits, int32_t n, int32_t batch,
                      int32_t* idx, int32_t* cnt, int32_t cap,
                      int32_t* union_idx, int32_t* union_cnt,

@@ -44,9 +44,12 @@ def layer(name):
     return _dev[name]
 
 
-def logits_bound(L, x, u_ref):
+def logits_bound(L, x, u_ref, split=False):
     """fp32 error bound of the GPU logits: stage-1 dot products of length d,
-    stage-2 of length r (+ bias), gamma_K = K u / (1 - K u), u = 2^-24."""
+    stage-2 of length r (+ bias), gamma_K = K u / (1 - K u), u = 2^-24.
+    split: stage 2 ran on the tensor cores with u as a high + low 16-bit
+    pair (batch > 1), which leaves |u - hi - lo| <= 2^-22 |u| (+ 2^-25 for
+    the f16 subnormal range of lo) for f16 and 2^-16 |u| for bf16."""
     uu = 2.0**-24
     g = lambda k: k * uu / (1 - k * uu)
     dec = (lambda b: b.view(np.float16).astype(np.float64)) if L.dtype == "f16" else \
@@ -54,7 +57,10 @@ def logits_bound(L, x, u_ref):
     A = np.abs(dec(L.A))
     B = np.abs(dec(L.Bm))
     du = g(L.d) * (B @ np.abs(x.astype(np.float64)))
-    return 2.0 * (A @ du + g(L.r + 1) * (A @ np.abs(u_ref) + np.abs(L.b1))) + 1e-30
+    au = np.abs(u_ref)
+    if split:
+        du = du + (2.0**-22 * au + 2.0**-25 if L.dtype == "f16" else 2.0**-16 * au)
+    return 2.0 * (A @ du + g(L.r + 1) * (A @ au + np.abs(L.b1))) + 1e-30
 
 
 # ---------------------------------------------------------------- predictor
@@ -71,8 +77,9 @@ def test_predict_parity(name, batch):
     torch.cuda.synchronize()
     g = lg.cpu().numpy().astype(np.float64)
     u, lo = oracle.predict(L, x)
+    split = batch > 1 and L.r % 16 == 0  # the batched predictor's tensor-core stage 2
     for t in range(batch):
-        bound = logits_bound(L, x[t], u[t])
+        bound = logits_bound(L, x[t], u[t], split)
         assert np.all(np.abs(g[t] - lo[t]) <= bound)
         tie = near_ties(lo[t])
         np.testing.assert_array_equal((g[t] > 0)[~tie], (lo[t] > 0)[~tie])
@@ -88,11 +95,15 @@ def test_predict_batch32_opt13b_shape():
     g = lg.cpu().numpy().astype(np.float64)
     u, lo = oracle.predict(L, x)
     for t in (0, 13, 31):
-        assert np.all(np.abs(g[t] - lo[t]) <= logits_bound(L, x[t], u[t]))
+        assert np.all(np.abs(g[t] - lo[t]) <= logits_bound(L, x[t], u[t], split=True))
+        tie = near_ties(lo[t])
+        np.testing.assert_array_equal((g[t] > 0)[~tie], (lo[t] > 0)[~tie])
 
 
 # ---------------------------------------------------------------- compaction
-def _compact(lg_host, cap, union=False, dev_status=True):
+def _compact(lg_host, cap, union=False, dev_status=True, grid=False):
+    """grid: pass a workspace, so that the grid-wide compaction runs (else
+    the one-block-per-token kernels)."""
     batch, n = lg_host.shape
     lg = up(lg_host.astype(np.float32), DEV)
     idx = torch.full((batch, max(cap, 1)), -7, dtype=torch.int32, device=DEV)
@@ -101,8 +112,9 @@ def _compact(lg_host, cap, union=False, dev_status=True):
     ui = torch.full((n,), -7, dtype=torch.int32, device=DEV) if union else None
     uc = zeros_i32(1, DEV) if union else None
     tm = torch.zeros(n, dtype=torch.int32, device=DEV) if union else None
+    ws = pi.workspace(pi.make_desc(8, n, 8), batch, DEV) if grid else None
     pi.check(pi.pi_compact(lg, n, batch, idx, cnt, cap, ui, uc, tm, st if dev_status else None,
-                           None, 0))
+                           ws, ws.numel() if grid else 0))
     torch.cuda.synchronize()
     out = dict(idx=idx.cpu().numpy(), cnt=cnt.cpu().numpy()[:batch], status=int(st[0]))
     if union:
@@ -111,14 +123,15 @@ def _compact(lg_host, cap, union=False, dev_status=True):
     return out
 
 
-@pytest.mark.parametrize("n", [1, 31, 1023, 1024, 1025, 4096, 28672, 100003])
-def test_compact_bit_exact(n):
+@pytest.mark.parametrize("grid", [False, True])
+@pytest.mark.parametrize("n", [1, 31, 255, 256, 257, 1023, 1024, 1025, 4096, 28672, 100003])
+def test_compact_bit_exact(n, grid):
     rng = np.random.default_rng(n)
     for density in (0.0, 0.07, 0.5, 1.0):
         lg = np.where(rng.random((3, n)) < density, rng.random((3, n)) + 1e-3,
                       -rng.random((3, n))).astype(np.float32)
         lg[:, : min(n, 3)] = [0.0, -0.0, 1e-38][: min(n, 3)]  # zeros are inactive
-        o = _compact(lg, n)
+        o = _compact(lg, n, grid=grid)
         assert o["status"] == 0
         for t in range(3):
             want = oracle.compact(lg[t].astype(np.float64))
@@ -126,24 +139,31 @@ def test_compact_bit_exact(n):
             np.testing.assert_array_equal(o["idx"][t][: len(want)], want)
 
 
-def test_compact_capacity_overflow_reported():
+@pytest.mark.parametrize("grid", [False, True])
+def test_compact_capacity_overflow_reported(grid):
     lg = np.ones((2, 5000), np.float32)
     lg[1, ::2] = -1.0
-    o = _compact(lg, 1000)
+    o = _compact(lg, 1000, grid=grid)
     assert o["status"] == pi.PI_ERR_CAPACITY
     assert list(o["cnt"]) == [5000, 2500]
     np.testing.assert_array_equal(o["idx"][0], np.arange(1000))
     np.testing.assert_array_equal(o["idx"][1], np.arange(1, 2001, 2))
 
 
+@pytest.mark.parametrize("grid", [False, True])
 @pytest.mark.parametrize("batch", [1, 4, 16, 32])
-def test_union_bit_exact(batch):
+def test_union_bit_exact(batch, grid):
     rng = np.random.default_rng(batch)
-    lg = (rng.standard_normal((batch, 20480)) - 1.8).astype(np.float32)
-    o = _compact(lg, 20480, union=True)
-    want_i, want_m = oracle.union(lg.astype(np.float64))
-    np.testing.assert_array_equal(o["uidx"], want_i)
-    np.testing.assert_array_equal(o["tmask"], want_m)
+    for n in (20480, 777):
+        lg = (rng.standard_normal((batch, n)) - 1.8).astype(np.float32)
+        o = _compact(lg, n, union=True, grid=grid)
+        want_i, want_m = oracle.union(lg.astype(np.float64))
+        np.testing.assert_array_equal(o["uidx"], want_i)
+        np.testing.assert_array_equal(o["tmask"], want_m)
+        for t in range(batch):  # and every token's own list
+            want = oracle.compact(lg[t].astype(np.float64))
+            assert o["cnt"][t] == len(want)
+            np.testing.assert_array_equal(o["idx"][t][: len(want)], want)
 
 
 # ---------------------------------------------------------------- sparse / dense FFN
