@@ -24,7 +24,7 @@ namespace pik {
 
 constexpr int kBT = 64;          // union neurons per phase-1 tile
 constexpr int kBK = 128;         // columns per phase-1 chunk
-constexpr int kBStages = 3;      // cp.async pipeline depth
+constexpr int kBStages = 3;      // cp.async pipeline depth (measured: deeper was not faster)
 constexpr int kBN2 = 32;         // union neurons per phase-2 chunk
 constexpr int kGroups2 = 8;      // neuron groups of phase 2
 
@@ -144,23 +144,33 @@ __global__ void __launch_bounds__(256) bpu_partial_kernel(const uint16_t* Bm, co
   }
 }
 
-// u[t][k] = sum_c part[c][t][k] (c ascending), then its high / low 16-bit
-// parts for the tensor cores ([bp][r]; zero rows for padded tokens).
+// u[t][k] = sum_c part[c][t][k], then its high / low 16-bit parts for the
+// tensor cores ([bp][r]; zero rows for padded tokens).  Block = 32 outputs
+// e = t r + k (consecutive, so every load of a warp is one 128-byte line);
+// warp w sums c = w, w + 8, ...; the 8 warp sums are added in warp order.
 template <int DT>
 __global__ void __launch_bounds__(256) bpu_reduce_kernel(const float* part, int r, int batch, int bp,
                                                          int G, uint16_t* uhi, uint16_t* ulo) {
-  const int e = blockIdx.x * 256 + threadIdx.x;  // t * r + k
-  if (e >= bp * r) return;
-  const int t = e / r, k = e - t * r;
+  __shared__ float ws[8][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 32 + lane;  // t * r + k
+  const int tot = batch * r;             // partials hold the real tokens only
   float s = 0.f;
-  if (t < batch) {
-#pragma unroll 8
-    for (int c = 0; c < G; ++c) s += part[((size_t)c * batch + t) * r + k];
+  if (e < tot) {
+#pragma unroll 4
+    for (int c = warp; c < G; c += 8) s += part[(size_t)c * tot + e];
   }
-  uint16_t hi, lo;
-  split16<DT>(s, &hi, &lo);
-  uhi[e] = hi;
-  ulo[e] = lo;
+  ws[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0 && e < bp * r) {
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) v += ws[w][lane];
+    uint16_t hi, lo;
+    split16<DT>(v, &hi, &lo);  // padded tokens (e >= tot): 0
+    uhi[e] = hi;
+    ulo[e] = lo;
+  }
 }
 
 // logits[t][i] = A_i . u[t] + b1_i on the tensor cores: block = 64 neurons x
@@ -267,14 +277,15 @@ __global__ void __launch_bounds__(512, 1) bup_kernel(const BatchArgs a) {
   const int kpar = (MT == 2) ? 0 : (warp >> 3);
   const int ksteps = kBK / 16;
   const int nchunks = a.d / kBK;
-  float* comb = reinterpret_cast<float*>(smem + kBStages * stage_bytes);  // [8][32][4 * NW]
+  constexpr int S = kBStages;
+  float* comb = reinterpret_cast<float*>(smem + S * stage_bytes);  // [8][32][4 * NW]
   const size_t w1s = a.packed ? (size_t)a.rec : (GATED ? 2 * (size_t)a.d : (size_t)a.d);
 
   for (int t0 = lo_u; t0 < hi_u; t0 += kBT) {
     const int tn = min(kBT, hi_u - t0);
-    // issue the cp.async loads of chunk ch into stage ch % kBStages
+    // issue the cp.async loads of chunk ch into stage ch % S
     auto issue = [&](int ch) {
-      unsigned char* st = smem + (ch % kBStages) * stage_bytes;
+      unsigned char* st = smem + (ch % S) * stage_bytes;
       const int k0 = ch * kBK;
       constexpr int CPR = kBK / 8;  // 16-byte pieces per row
       for (int e = tid; e < NW * kBT * CPR; e += 512) {
@@ -301,16 +312,16 @@ __global__ void __launch_bounds__(512, 1) bup_kernel(const BatchArgs a) {
     for (int w = 0; w < NW; ++w)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[w][e] = 0.f;
-    for (int ch = 0; ch < kBStages - 1; ++ch) {  // always kBStages - 1 groups
+    for (int ch = 0; ch < S - 1; ++ch) {  // always S - 1 groups
       if (ch < nchunks) issue(ch);
       cp_async_commit();
     }
     for (int ch = 0; ch < nchunks; ++ch) {
-      if (ch + kBStages - 1 < nchunks) issue(ch + kBStages - 1);
+      if (ch + S - 1 < nchunks) issue(ch + S - 1);
       cp_async_commit();
       asm volatile("cp.async.wait_group %0;" ::"n"(kBStages - 1) : "memory");
       __syncthreads();
-      const unsigned char* st = smem + (ch % kBStages) * stage_bytes;
+      const unsigned char* st = smem + (ch % S) * stage_bytes;
       const unsigned char* xs_ = st + (size_t)NW * kBT * kRowB;
       for (int ks = kpar; ks < ksteps; ks += (MT == 2 ? 1 : 2)) {
         uint32_t ah[4], al[4];
@@ -400,6 +411,7 @@ __global__ void __launch_bounds__(512, 1) bdown_kernel(const BatchArgs a) {
   const int NT = cn / 8;
   const int w2row = bdn_w2_row(a.cw);
   const int stage_bytes = bdn_stage_bytes(a.cw, a.bp);
+  constexpr int S = kBStages;
   const size_t w2s = a.packed ? (size_t)a.rec : (size_t)a.d;  // W2 rows (packed: inside records)
   const uint16_t* w2base = a.W2;
   // warp w owns n tiles w, w + 16, w + 32 (< NT), all m tiles
@@ -413,7 +425,7 @@ __global__ void __launch_bounds__(512, 1) bdown_kernel(const BatchArgs a) {
       for (int e = 0; e < 4; ++e) acc[q][m][e] = 0.f;
   const int nchunks = (hi_u - lo_u + kBN2 - 1) / kBN2;
   auto issue = [&](int ch) {
-    unsigned char* st = smem + (ch % kBStages) * stage_bytes;
+    unsigned char* st = smem + (ch % S) * stage_bytes;
     const int p0 = lo_u + ch * kBN2;
     const int cpr = cn / 8;  // 16-byte pieces per W2 row piece
     for (int e = tid; e < kBN2 * cpr; e += 512) {
@@ -453,16 +465,16 @@ __global__ void __launch_bounds__(512, 1) bdown_kernel(const BatchArgs a) {
       }
     }
   };
-  for (int ch = 0; ch < kBStages - 1; ++ch) {  // always kBStages - 1 groups
+  for (int ch = 0; ch < S - 1; ++ch) {  // always S - 1 groups
     if (ch < nchunks) issue(ch);
     cp_async_commit();
   }
   for (int ch = 0; ch < nchunks; ++ch) {
-    if (ch + kBStages - 1 < nchunks) issue(ch + kBStages - 1);
+    if (ch + S - 1 < nchunks) issue(ch + S - 1);
     cp_async_commit();
     asm volatile("cp.async.wait_group %0;" ::"n"(kBStages - 1) : "memory");
     __syncthreads();
-    const unsigned char* st = smem + (ch % kBStages) * stage_bytes;
+    const unsigned char* st = smem + (ch % S) * stage_bytes;
     const unsigned char* hs_ = st + (size_t)kBN2 * w2row;
 #pragma unroll
     for (int ks = 0; ks < kBN2 / 16; ++ks) {

@@ -564,7 +564,7 @@ pi_status pi_predict(const pi_ffn_desc* desc, const void* A, const void* Bm, con
     }
     if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
     const int bp = L.bp;
-    const unsigned gr = (unsigned)((bp * D.r + 255) / 256);
+    const unsigned gr = (unsigned)((bp * D.r + 31) / 32);
     if (!bf) bpu_reduce_kernel<0><<<gr, 256, 0, st>>>(part, D.r, batch, bp, G, uhi, ulo);
     else bpu_reduce_kernel<1><<<gr, 256, 0, st>>>(part, D.r, batch, bp, G, uhi, ulo);
     if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
