@@ -63,6 +63,12 @@ def lib():
             L.or_layer_decode.restype = i32
             L.or_layer_decode.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp,
                                           vp, vp, vp, vp]
+            L.or_profile_counts.restype = None
+            L.or_profile_counts.argtypes = [vp, i32, i32, vp]
+            L.or_hot_order.restype = None
+            L.or_hot_order.argtypes = [vp, i32, vp]
+            L.or_permute_rows.restype = None
+            L.or_permute_rows.argtypes = [vp, i32, i32, vp, vp]
             L.or_set_threads.restype = None
             L.or_set_threads.argtypes = [i32]
             L.or_get_threads.restype = i32
@@ -177,3 +183,35 @@ def layer_decode(layer, x, residual: bool = False):
                               _p(layer.A), _p(layer.Bm), _p(layer.b1), _p(layer.W1),
                               _p(layer.W2), _p(layer.b2), _p(x), _p(lg), _p(idx), _p(y), _p(xn))
     return lg, idx[:c].copy(), y, xn
+
+
+# ------------------------------------------------------------ offline placement
+def profile_counts(logits, counts=None):
+    """Activation counts per neuron over the tokens of logits [batch, n]
+    (added to counts if given): the profiler of the page's "Offline
+    Section"."""
+    lg = np.ascontiguousarray(np.atleast_2d(logits), dtype=np.float64)
+    batch, n = lg.shape
+    c = np.zeros(n, np.uint32) if counts is None else np.ascontiguousarray(counts, np.uint32)
+    lib().or_profile_counts(_p(lg), n, batch, _p(c))
+    return c
+
+
+def hot_order(counts):
+    """perm[k] = original neuron placed at position k: more activations
+    first, equal counts in ascending index (the neuron table)."""
+    c = np.ascontiguousarray(counts, np.uint32)
+    perm = np.empty(c.shape[0], np.int32)
+    lib().or_hot_order(_p(c), c.shape[0], _p(perm))
+    return perm
+
+
+def permute_rows(rows, perm):
+    """Row k of the result = row perm[k] of rows (any dtype, one row per
+    neuron)."""
+    src = np.ascontiguousarray(rows)
+    dst = np.empty_like(src)
+    n = src.shape[0]
+    rb = src.nbytes // max(n, 1)
+    lib().or_permute_rows(_p(src), n, rb, _p(np.ascontiguousarray(perm, np.int32)), _p(dst))
+    return dst

@@ -8,6 +8,7 @@
 
 #include <math.h>
 #include <stdlib.h>
+#include <string.h>
 #ifdef _OPENMP
 #include <omp.h>
 #endif
@@ -193,4 +194,45 @@ int32_t or_layer_decode(int32_t d, int32_t n, int32_t r, int32_t dtype,
   if (x_next)
     for (int32_t j = 0; j < d; ++j) x_next[j] = (float)((double)x[j] + y[j]);
   return cnt;
+}
+
+/* ------------------------------------------------------------ offline placement */
+void or_profile_counts(const double* logits, int32_t n, int32_t batch,
+                       uint32_t* counts) {
+  for (int32_t t = 0; t < batch; ++t)
+    for (int32_t i = 0; i < n; ++i)
+      if (logits[(size_t)t * n + i] > 0.0) counts[i] += 1u;
+}
+
+typedef struct {
+  uint32_t count;
+  int32_t index;
+} or_key;
+
+/* more activations first; equal counts by ascending index */
+static int or_key_cmp(const void* pa, const void* pb) {
+  const or_key* a = (const or_key*)pa;
+  const or_key* b = (const or_key*)pb;
+  if (a->count != b->count) return a->count > b->count ? -1 : 1;
+  return (a->index > b->index) - (a->index < b->index);
+}
+
+void or_hot_order(const uint32_t* counts, int32_t n, int32_t* perm) {
+  or_key* k = (or_key*)malloc(sizeof(or_key) * (size_t)(n > 0 ? n : 1));
+  if (!k) return;
+  for (int32_t i = 0; i < n; ++i) {
+    k[i].count = counts[i];
+    k[i].index = i;
+  }
+  qsort(k, (size_t)n, sizeof(or_key), or_key_cmp);
+  for (int32_t i = 0; i < n; ++i) perm[i] = k[i].index;
+  free(k);
+}
+
+void or_permute_rows(const void* src, int32_t n, int32_t row_bytes,
+                     const int32_t* perm, void* dst) {
+  const unsigned char* s = (const unsigned char*)src;
+  unsigned char* d = (unsigned char*)dst;
+  for (int32_t k = 0; k < n; ++k)
+    memcpy(d + (size_t)k * row_bytes, s + (size_t)perm[k] * row_bytes, (size_t)row_bytes);
 }

@@ -94,6 +94,21 @@ int32_t or_layer_decode(int32_t d, int32_t n, int32_t r, int32_t dtype,
                         double* logits, int32_t* idx, double* y,
                         float* x_next);
 
+/* Offline profiling and neuron placement ("Offline Section": a profiler
+ * records how often each neuron activates over sample inputs, and the
+ * neurons are placed hot first; "Neuron Placement and Administration": the
+ * neuron table maps a neuron's placed position to its original one).
+ *   or_profile_counts: counts[i] += #{t < batch : logits[t][i] > 0}
+ *     (logits [batch][n]).
+ *   or_hot_order: perm[k] = the original neuron placed at position k: more
+ *     activations first, equal counts in ascending original index.
+ *   or_permute_rows: dst row k = src row perm[k], rows of row_bytes bytes. */
+void or_profile_counts(const double* logits, int32_t n, int32_t batch,
+                       uint32_t* counts);
+void or_hot_order(const uint32_t* counts, int32_t n, int32_t* perm);
+void or_permute_rows(const void* src, int32_t n, int32_t row_bytes,
+                     const int32_t* perm, void* dst);
+
 void or_set_threads(int32_t nthreads);
 int32_t or_get_threads(void);
 

@@ -302,3 +302,94 @@ def test_thread_count_does_not_change_results():
     for u, v in zip(a[:3], b[:3]):
         np.testing.assert_array_equal(u, v)
     np.testing.assert_array_equal(b1, b2)
+
+
+# ---------------------------------------------------------------- offline placement
+def test_profile_counts_brute_force():
+    rng = np.random.default_rng(7)
+    lg = rng.standard_normal((5, 37))
+    lg[0, :4] = [0.0, -0.0, 1e-300, -1e-300]  # only the positive one counts
+    c = oracle.profile_counts(lg)
+    want = [sum(1 for t in range(5) if lg[t, i] > 0) for i in range(37)]
+    assert c.tolist() == want
+    assert c[0] == sum(1 for t in range(1, 5) if lg[t, 0] > 0)
+    # counts accumulate over calls
+    c2 = oracle.profile_counts(lg, c)
+    assert c2.tolist() == [2 * v for v in want]
+
+
+def test_hot_order_hand_worked():
+    # counts 3 5 5 0 3 7 -> 7 (neuron 5), then the two 5s by index (1, 2),
+    # the two 3s (0, 4), then 0 (3)
+    assert oracle.hot_order(np.array([3, 5, 5, 0, 3, 7])).tolist() == [5, 1, 2, 0, 4, 3]
+    assert oracle.hot_order(np.zeros(6)).tolist() == list(range(6))
+    assert oracle.hot_order(np.array([9])).tolist() == [0]
+
+
+def test_hot_order_properties_with_many_ties():
+    rng = np.random.default_rng(8)
+    c = rng.integers(0, 6, 2000).astype(np.uint32)
+    p = oracle.hot_order(c)
+    assert sorted(p.tolist()) == list(range(2000))          # a permutation
+    cp = c[p]
+    assert np.all(np.diff(cp.astype(np.int64)) <= 0)        # hot first
+    same = np.diff(cp.astype(np.int64)) == 0
+    assert np.all(np.diff(p)[same] > 0)                     # ties keep index order
+    want = [i for _, i in sorted((-int(v), i) for i, v in enumerate(c))]
+    assert p.tolist() == want
+
+
+def test_permute_rows_and_inverse():
+    rng = np.random.default_rng(9)
+    rows = rng.integers(0, 2**16, (50, 24)).astype(np.uint16)
+    perm = rng.permutation(50).astype(np.int32)
+    out = oracle.permute_rows(rows, perm)
+    for k in range(50):
+        assert np.array_equal(out[k], rows[perm[k]])
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(50, dtype=np.int32)
+    assert np.array_equal(oracle.permute_rows(out, inv), rows)
+    b = rng.standard_normal(50).astype(np.float32)
+    assert np.array_equal(oracle.permute_rows(b, perm), b[perm])
+
+
+def _oracle_permuted(L, perm):
+    return synth.Layer(L.d, L.n, L.r, L.dtype, L.gated, oracle.permute_rows(L.A, perm), L.Bm,
+                       oracle.permute_rows(L.b1, perm), oracle.permute_rows(L.W1, perm),
+                       oracle.permute_rows(L.W2, perm), L.b2, dict(L.meta))
+
+
+def test_placement_keeps_the_decode_and_maps_the_table():
+    # A layer stored in a random order, profiled and placed hot first,
+    # decodes to the same y; its active list maps back through the table.
+    L = synth.make_layer(64, 300, 8, "f16", alpha=0.9, density=0.2, seed=10)
+    rng = np.random.default_rng(10)
+    shuf = rng.permutation(300).astype(np.int32)
+    Ls = _oracle_permuted(L, shuf)
+    xs = synth.gen_x(10, 0, 40, 64)
+    _, lg = oracle.predict(Ls, xs)
+    perm = oracle.hot_order(oracle.profile_counts(lg))
+    Lp = _oracle_permuted(Ls, perm)
+    for t in range(3):
+        x = synth.gen_x(11, t, 1, 64)[0]
+        _, _, ys, _ = oracle.layer_decode(Ls, x)
+        lgp, idxp, yp, _ = oracle.layer_decode(Lp, x)
+        np.testing.assert_allclose(yp, ys, rtol=0, atol=1e-12 * max(1.0, np.abs(ys).max()))
+        _, ids, _, _ = oracle.layer_decode(Ls, x)
+        assert sorted(perm[idxp].tolist()) == sorted(ids.tolist())
+
+
+def test_placement_recovers_hot_first_order():
+    # the generated layer is hot first; shuffled, then profiled over 400
+    # tokens and placed, the activation rate falls along the new order
+    L = synth.make_layer(64, 512, 8, "f16", alpha=0.9, density=0.1, seed=12)
+    shuf = np.random.default_rng(12).permutation(512).astype(np.int32)
+    Ls = _oracle_permuted(L, shuf)
+    c = np.zeros(512, np.uint32)
+    for s in range(10):
+        _, lg = oracle.predict(Ls, synth.gen_x(12, s, 40, 64))
+        c = oracle.profile_counts(lg, c)
+    perm = oracle.hot_order(c)
+    orig = shuf[perm]              # original (hot-first) index at each placed position
+    assert np.mean(orig[:50]) < 0.25 * np.mean(orig[-200:])
+    assert np.all(np.diff(c[perm].astype(np.int64)) <= 0)
