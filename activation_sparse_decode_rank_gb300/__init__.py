@@ -86,6 +86,9 @@ SIGNATURES = {
     "pi_layer_decode_static": (ctypes.c_int, [_DESC, _W, _P, _P, _P, _P, _P, _P, _P]),
     "pi_decode_layers": (ctypes.c_int, [_P, _P, _I32, _I32, _P, _I32, _P, _P, _P, _P, _P, _SZ,
                                         _P]),
+    "pi_profile_counts": (ctypes.c_int, [_P, _I32, _I32, _P, _P]),
+    "pi_hot_order": (ctypes.c_int, [_P, _I32, _P, _P]),
+    "pi_permute_neurons": (ctypes.c_int, [_DESC, _W, _P, _W, _P, _P]),
 }
 
 
@@ -207,6 +210,19 @@ def pi_decode_layers(descs, layers, J, x, chain, y, cnt_out, mask_out, dev_statu
                                   R, J, _ptr(x), chain, _ptr(y), _ptr(cnt_out), _ptr(mask_out),
                                   _ptr(dev_status), _ptr(ws),
                                   ws.numel() if ws_bytes is None else ws_bytes, _stream(stream))
+
+
+def pi_profile_counts(logits, n, batch, counts, stream=None) -> int:
+    return lib().pi_profile_counts(_ptr(logits), n, batch, _ptr(counts), _stream(stream))
+
+
+def pi_hot_order(counts, n, perm, stream=None) -> int:
+    return lib().pi_hot_order(_ptr(counts), n, _ptr(perm), _stream(stream))
+
+
+def pi_permute_neurons(desc, src, perm, dst, dev_status, stream=None) -> int:
+    return lib().pi_permute_neurons(ctypes.byref(desc), ctypes.byref(src), _ptr(perm),
+                                    ctypes.byref(dst), _ptr(dev_status), _stream(stream))
 
 
 def pi_pack_weights(desc, W1, W2, packed, stream=None) -> int:

@@ -961,6 +961,72 @@ __global__ void __launch_bounds__(kCB) cu_write_kernel(const float* logits, int 
   }
 }
 
+// ------------------------------------------------------------ offline placement
+// "Offline Section": a profiler counts how often each neuron activates over
+// sample inputs and the neurons are placed hot first; the placed layer's
+// row k is the original row perm[k] ("Neuron Placement and Administration":
+// perm is the neuron table).
+
+// counts[i] += #{t < batch : logits[t][i] > 0}; one thread per neuron.
+__global__ void profile_count_kernel(const float* logits, int n, int batch, unsigned* counts) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    unsigned c = 0u;
+    for (int t = 0; t < batch; ++t) c += logits[(size_t)t * n + i] > 0.f ? 1u : 0u;
+    counts[i] += c;
+  }
+}
+
+// perm[rank(i)] = i, rank(i) = #{j : c_j > c_i} + #{j < i : c_j == c_i}:
+// more activations first, equal counts in ascending index.  Each thread
+// compares its count with every count (tiles staged in shared memory).
+constexpr int kRankTile = 2048;
+__global__ void __launch_bounds__(256) rank_kernel(const unsigned* counts, int n, int* perm) {
+  __shared__ unsigned tile[kRankTile];
+  const int i = blockIdx.x * 256 + threadIdx.x;
+  const unsigned ci = i < n ? counts[i] : 0u;
+  int rank = 0;
+  for (int j0 = 0; j0 < n; j0 += kRankTile) {
+    const int m = min(kRankTile, n - j0);
+    __syncthreads();
+    for (int e = threadIdx.x; e < m; e += 256) tile[e] = counts[j0 + e];
+    __syncthreads();
+    for (int jj = 0; jj < m; ++jj) {
+      const unsigned cj = tile[jj];
+      rank += (cj > ci || (cj == ci && j0 + jj < i)) ? 1 : 0;
+    }
+  }
+  if (i < n) perm[rank] = i;
+}
+
+// dst row k = src row perm[k], rows of q16 sixteen-byte pieces.  An entry
+// outside [0, n) is not followed: the row is left alone and PI_ERR_INDEX
+// is recorded.
+__global__ void gather_rows16_kernel(const uint4* src, uint4* dst, const int* perm, int n,
+                                     long long q16, int* status) {
+  const long long tot = (long long)n * q16;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < tot;
+       e += (long long)gridDim.x * blockDim.x) {
+    const long long k = e / q16, q = e - k * q16;
+    const int pk = __ldg(perm + k);
+    if ((unsigned)pk >= (unsigned)n) {
+      if (q == 0) set_status(status, PI_ERR_INDEX);
+      continue;
+    }
+    dst[e] = __ldg(src + (long long)pk * q16 + q);
+  }
+}
+__global__ void gather_f32_kernel(const float* src, float* dst, const int* perm, int n,
+                                  int* status) {
+  for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < n; k += gridDim.x * blockDim.x) {
+    const int pk = __ldg(perm + k);
+    if ((unsigned)pk >= (unsigned)n) {
+      set_status(status, PI_ERR_INDEX);
+      continue;
+    }
+    dst[k] = __ldg(src + pk);
+  }
+}
+
 // Failure-path diagnostic: one grid-wide wait whose last arrival never
 // comes (expected = grid + 1), so every block gives up after limit_ns.
 __global__ void wait_timeout_kernel(unsigned long long* bar, int* status,

@@ -872,6 +872,65 @@ pi_status pi_decode_layers(const pi_ffn_desc* descs, const pi_layer_weights* lay
   return map_launch_error(cudaLaunchKernelEx(&cfg, fn, sa));
 }
 
+pi_status pi_profile_counts(const float* logits, int32_t n, int32_t batch, uint32_t* counts,
+                            pi_stream stream) {
+  if (n < 1 || n > (1 << 24) || batch < 1 || batch > kMaxBatch) return PI_ERR_SHAPE;
+  if (!logits || !counts) return PI_ERR_NULL;
+  if (!aligned16(logits) || !aligned16(counts)) return PI_ERR_ALIGN;
+  const unsigned grid = (unsigned)((n + 255) / 256);
+  profile_count_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      logits, n, batch, reinterpret_cast<unsigned*>(counts));
+  return cudaGetLastError() == cudaSuccess ? PI_OK : PI_ERR_CUDA;
+}
+
+pi_status pi_hot_order(const uint32_t* counts, int32_t n, int32_t* perm, pi_stream stream) {
+  if (n < 1 || n > (1 << 22)) return PI_ERR_SHAPE;
+  if (!counts || !perm) return PI_ERR_NULL;
+  if (!aligned16(counts) || !aligned16(perm)) return PI_ERR_ALIGN;
+  rank_kernel<<<(unsigned)((n + 255) / 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const unsigned*>(counts), n, perm);
+  return cudaGetLastError() == cudaSuccess ? PI_OK : PI_ERR_CUDA;
+}
+
+pi_status pi_permute_neurons(const pi_ffn_desc* desc, const pi_layer_weights* src,
+                             const int32_t* perm, const pi_layer_weights* dst,
+                             int32_t* dev_status, pi_stream stream) {
+  pi_status s = check_desc(desc);
+  if (s != PI_OK) return s;
+  if (!src || !dst || !perm || !dev_status) return PI_ERR_NULL;
+  const pi_ffn_desc& D = *desc;
+  s = check_weights(D, src, true);
+  if (s != PI_OK) return s;
+  s = check_weights(D, dst, true);
+  if (s != PI_OK) return s;
+  if (!aligned16(perm) || !aligned16(dev_status)) return PI_ERR_ALIGN;
+  // out of place only: every permuted tensor gets a buffer of its own
+  if (dst->A == src->A || dst->b1 == src->b1 || dst->W1 == src->W1 ||
+      (D.layout == PI_LAYOUT_SPLIT && dst->W2 == src->W2))
+    return PI_ERR_SHAPE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int m1 = D.gated ? 2 : 1;
+  const long long w1q = (D.layout == PI_LAYOUT_PACKED ? (long long)(m1 + 1) : m1) * D.d / 8;
+  struct Job {
+    const void* a;
+    void* b;
+    long long q16;
+  } jobs[3] = {{src->A, const_cast<void*>(dst->A), D.r / 8},
+               {src->W1, const_cast<void*>(dst->W1), w1q},
+               {src->W2, const_cast<void*>(dst->W2), D.d / 8}};
+  const int nj = D.layout == PI_LAYOUT_SPLIT ? 3 : 2;
+  for (int j = 0; j < nj; ++j) {
+    const long long tot = (long long)D.n * jobs[j].q16;
+    const long long blocks = (tot + 255) / 256;
+    gather_rows16_kernel<<<(unsigned)(blocks < 152 * 64 ? blocks : 152 * 64), 256, 0, st>>>(
+        static_cast<const uint4*>(jobs[j].a), static_cast<uint4*>(jobs[j].b), perm, D.n,
+        jobs[j].q16, dev_status);
+  }
+  gather_f32_kernel<<<(unsigned)((D.n + 255) / 256), 256, 0, st>>>(
+      src->b1, const_cast<float*>(dst->b1), perm, D.n, dev_status);
+  return cudaGetLastError() == cudaSuccess ? PI_OK : PI_ERR_CUDA;
+}
+
 pi_status pi_pack_weights(const pi_ffn_desc* desc, const void* W1, const void* W2, void* packed,
                           pi_stream stream) {
   pi_ffn_desc D = desc ? *desc : pi_ffn_desc{};

@@ -741,6 +741,87 @@ def run_sweep(args):
     return 0
 
 
+def run_reorder(args):
+    """Offline profiling and neuron placement, timed (one JSON line): the
+    GPU predictor over sample tokens plus pi_profile_counts (per token),
+    pi_hot_order, and pi_permute_neurons (bytes moved: every per-neuron
+    tensor read and written once, against the HBM peak)."""
+    import torch
+
+    import activation_sparse_decode_rank_gb300 as pi
+    import synth
+
+    rank, world, local = dist_env()
+    if rank != 0:
+        return 0
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pi.build()
+    w = workload_spec(args.workload)
+    d, n, r = w["d"], w["n"], w["r"]
+    gated = bool(w["gated"])
+    if "alpha" in w:
+        g = synth.make_layer_gpu(d, n, r, w["dtype"], gated=gated, alpha=w["alpha"],
+                                 density=w["density"], seed=w["seed"], device=dev)
+    else:  # a stack: its first layer
+        alpha, _, cz, scale = synth.stack_plan(w["seed"], w["layers"], n)
+        g = synth.make_layer_gpu(d, n, r, w["dtype"], gated=gated, alpha=float(alpha[0]),
+                                 zipf_c=float(cz[0]), seed=w["seed"], layer=0,
+                                 bias_scale=float(scale[0]), device=dev)
+    torch.cuda.synchronize()
+    desc = pi.make_desc(d, n, r, w["dtype"], gated, 0)
+    src = pi.make_weights(g["A"], g["Bm"], g["b1"], g["W1"], g["W2"], g["b2"])
+    B, T = 32, 256
+    ws = pi.workspace(desc, B, dev)
+    xs = torch.from_numpy(np.stack([synth.gen_x(w["seed"] + 77, s, B, d)
+                                    for s in range(T // B)])).to(dev)
+    lg = torch.empty((B, n), dtype=torch.float32, device=dev)
+    counts = torch.zeros(n, dtype=torch.int32, device=dev)
+    perm = torch.empty(n, dtype=torch.int32, device=dev)
+    dst_t = [torch.empty_like(g["A"]), torch.empty_like(g["b1"]), torch.empty_like(g["W1"]),
+             torch.empty_like(g["W2"])]
+    dst = pi.make_weights(dst_t[0], g["Bm"], dst_t[1], dst_t[2], dst_t[3], g["b2"])
+    st = torch.zeros(4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def timed(fn, reps):
+        with torch.cuda.stream(stream):
+            fn()
+            stream.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+            stream.synchronize()
+        return e0.elapsed_time(e1) / reps * 1e3  # us
+
+    def profile():
+        for s in range(T // B):
+            pi.check(pi.pi_predict(desc, g["A"], g["Bm"], g["b1"], xs[s], B, lg, ws, stream=stream))
+            pi.check(pi.pi_profile_counts(lg, n, B, counts, stream=stream))
+
+    us_prof = timed(profile, 5)
+    us_rank = timed(lambda: pi.check(pi.pi_hot_order(counts, n, perm, stream=stream)), 5)
+    us_perm = timed(lambda: pi.check(pi.pi_permute_neurons(desc, src, perm, dst, st,
+                                                           stream=stream)), 10)
+    if int(st[0]) != 0:
+        raise SystemExit(f"bench: device status {pi.status_string(int(st[0]))}")
+    moved = 2 * sum(t.numel() * t.element_size() for t in dst_t)
+    peak, peak_kind = measured_peaks()
+    print(json.dumps({
+        "metric": "offline profiling and neuron placement", "workload": args.workload,
+        "config": {"d": d, "n": n, "r": r, "weights": w["dtype"], "gated": gated,
+                   "sample_tokens": T, "predictor_batch": B},
+        "profile_us_per_token": us_prof / T, "hot_order_us": us_rank,
+        "permute_us": us_perm, "permute_bytes": moved,
+        "permute_gbs": moved / us_perm / 1e3, "permute_frac": moved / us_perm / 1e3 / peak,
+        "peak_gbs": peak, "peak_kind": peak_kind, "csrc_hash": csrc_hash(),
+    }), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -759,6 +840,8 @@ def main():
                          "pi_decode_layers, one persistent launch per graph-length chunk of "
                          "steps (per token for a stack); auto: seq for one layer, call for "
                          "a stack (the faster of the two on each, as measured on GB300)")
+    ap.add_argument("--reorder", action="store_true",
+                    help="offline profiling + neuron placement timings for --workload")
     ap.add_argument("--sweep", action="store_true",
                     help="batched decode / density sweep (with --workload opt13b_ffn_batched_...)")
     args = ap.parse_args()
@@ -768,6 +851,8 @@ def main():
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
+    if args.reorder:
+        return run_reorder(args)
     stack = workload_spec(args.workload).get("layers", 1) > 1
     if args.engine == "auto":
         args.engine = "call" if stack else "seq"

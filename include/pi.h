@@ -250,6 +250,35 @@ pi_status pi_layer_decode_static(const pi_ffn_desc* desc, const pi_layer_weights
                                  int32_t* idx_out, int32_t* cnt_out, int32_t* dev_status,
                                  pi_stream stream);
 
+/* Offline profiling and neuron placement ("Offline Section": a profiler
+ * records how often each neuron activates over sample inputs, and the
+ * neurons are placed so that the hot ones come first; "Neuron Placement and
+ * Administration": a neuron table maps each placed position to the neuron's
+ * original one).  Run before decoding, on the caller's stream:
+ *   pi_profile_counts: counts[i] += #{t < batch : logits[t][i] > 0} for
+ *     logits [batch][n] fp32 (e.g. from pi_predict over sample tokens);
+ *     counts [n] uint32 accumulate across calls (zero them first).
+ *     n <= 2^24, batch <= 32.
+ *   pi_hot_order: perm[k] = the original neuron placed at position k: more
+ *     activations first, equal counts in ascending index.  perm [n] int32
+ *     is the neuron table.  n <= 2^22 (each entry is ranked against every
+ *     count: O(n^2) work, a fraction of a millisecond at n = 28 672).
+ *   pi_permute_neurons: dst row k = src row perm[k] for A, b1, W1 (gated:
+ *     gate|up rows; packed: whole records) and W2 (split layout); dst holds
+ *     buffers of the same sizes, distinct from src (PI_ERR_SHAPE otherwise);
+ *     dst->Bm and dst->b2 are not written (Bm is not per neuron; they may
+ *     be src's).  perm must be a permutation of [0, n): an entry outside
+ *     [0, n) is not followed, its row is left unwritten and PI_ERR_INDEX is
+ *     written to *dev_status.  Decoding the placed layer gives the same y;
+ *     its active list maps to original neurons through perm. */
+pi_status pi_profile_counts(const float* logits, int32_t n, int32_t batch,
+                            uint32_t* counts, pi_stream stream);
+pi_status pi_hot_order(const uint32_t* counts, int32_t n, int32_t* perm,
+                       pi_stream stream);
+pi_status pi_permute_neurons(const pi_ffn_desc* desc, const pi_layer_weights* src,
+                             const int32_t* perm, const pi_layer_weights* dst,
+                             int32_t* dev_status, pi_stream stream);
+
 /* Offline step: builds the PI_LAYOUT_PACKED records of a layer from its
  * split matrices (desc->layout is ignored).  W1 [n][d] (gated [n][2][d]) and
  * W2 [n][d] are read, packed [n][m d] is written (m = 2, or 3 if gated); the

@@ -144,6 +144,28 @@ def test_decode_layers_host_validation(lib):
     assert f([d], [w], 1, P, 1, P, None, None, P, P, wsb - 256) == pi.PI_ERR_WORKSPACE
 
 
+def test_placement_host_validation(lib):
+    P = 1 << 40
+    L = lib
+    by = ctypes.byref
+    assert L.pi_profile_counts(P, 0, 1, P, None) == pi.PI_ERR_SHAPE
+    assert L.pi_profile_counts(P, 10, 33, P, None) == pi.PI_ERR_SHAPE
+    assert L.pi_profile_counts(None, 10, 1, P, None) == pi.PI_ERR_NULL
+    assert L.pi_profile_counts(P, 10, 1, P + 4, None) == pi.PI_ERR_ALIGN
+    assert L.pi_hot_order(P, 0, P, None) == pi.PI_ERR_SHAPE
+    assert L.pi_hot_order(P, (1 << 22) + 1, P, None) == pi.PI_ERR_SHAPE
+    assert L.pi_hot_order(P, 10, None, None) == pi.PI_ERR_NULL
+    d = pi.make_desc(1024, 4096, 64, "f16")
+    w = pi.make_weights(P, P, P, P, P, None)
+    w2 = pi.make_weights(P + 4096, P, P + 8192, P + 16384, P + 32768, None)
+    assert L.pi_permute_neurons(by(d), by(w), P, by(w2), None, None) == pi.PI_ERR_NULL
+    assert L.pi_permute_neurons(by(d), by(w), None, by(w2), P, None) == pi.PI_ERR_NULL
+    assert L.pi_permute_neurons(by(d), by(w), P + 4, by(w2), P, None) == pi.PI_ERR_ALIGN
+    assert L.pi_permute_neurons(by(d), by(w), P, by(w), P, None) == pi.PI_ERR_SHAPE  # in place
+    wbad = pi.make_weights(P, P, P, P, None, None)
+    assert L.pi_permute_neurons(by(d), by(w), P, by(wbad), P, None) == pi.PI_ERR_NULL
+
+
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(pi, "_LIB", str(tmp_path / "missing.so"))
     monkeypatch.setattr(pi, "_lib", None)
