@@ -23,9 +23,9 @@
 namespace pik {
 
 constexpr int kBT = 64;          // union neurons per phase-1 tile
-constexpr int kBK = 128;         // columns per phase-1 chunk
+constexpr int kBK = 128;         // columns per phase-1 chunk (256 for plain layers, d % 256 == 0)
 constexpr int kBStages = 3;      // cp.async pipeline depth (measured: deeper was not faster)
-constexpr int kBN2 = 32;         // union neurons per phase-2 chunk
+constexpr int kBN2 = 64;         // union neurons per phase-2 chunk
 constexpr int kGroups2 = 8;      // neuron groups of phase 2
 
 struct BatchArgs {
@@ -254,29 +254,32 @@ __global__ void bsplit_x_kernel(const BatchArgs a) {
 // Shared-memory layout of one pipeline stage: W1 rows [kBT][kBK] (gated:
 // gate rows then up rows), then x high / low parts [bp][kBK]; rows padded by
 // 16 bytes.
-constexpr int kRowB = kBK * 2 + 16;  // bytes per staged row
-
-template <bool GATED>
+template <int BK>
+__host__ __device__ constexpr int bup_row_bytes() {
+  return BK * 2 + 16;  // bytes per staged row
+}
+template <bool GATED, int BK>
 __host__ __device__ constexpr int bup_stage_bytes(int bp) {
-  return ((GATED ? 2 : 1) * kBT + 2 * bp) * kRowB;
+  return ((GATED ? 2 : 1) * kBT + 2 * bp) * bup_row_bytes<BK>();
 }
 
-template <int DT, bool GATED, int MT>
+template <int DT, bool GATED, int MT, int BK>
 __global__ void __launch_bounds__(512, 1) bup_kernel(const BatchArgs a) {
+  constexpr int kRowB = bup_row_bytes<BK>();
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int U = a.dense ? a.n : __ldg(a.ucnt);
   const int lo_u = (int)((long long)blockIdx.x * U / a.P);
   const int hi_u = (int)((long long)(blockIdx.x + 1) * U / a.P);
-  const int stage_bytes = bup_stage_bytes<GATED>(a.bp);
+  const int stage_bytes = bup_stage_bytes<GATED, BK>(a.bp);
   constexpr int NW = GATED ? 2 : 1;
   // warp -> (m tile, n tile, k parity): MT = 2: 16 fragments, one per warp;
   // MT = 1: 8 fragments, two warps each, taking alternate k-steps.
   const int nt = warp & 7;
   const int mt = (MT == 2) ? (warp >> 3) : 0;
   const int kpar = (MT == 2) ? 0 : (warp >> 3);
-  const int ksteps = kBK / 16;
-  const int nchunks = a.d / kBK;
+  const int ksteps = BK / 16;
+  const int nchunks = a.d / BK;
   constexpr int S = kBStages;
   float* comb = reinterpret_cast<float*>(smem + S * stage_bytes);  // [8][32][4 * NW]
   const size_t w1s = a.packed ? (size_t)a.rec : (GATED ? 2 * (size_t)a.d : (size_t)a.d);
@@ -286,8 +289,8 @@ __global__ void __launch_bounds__(512, 1) bup_kernel(const BatchArgs a) {
     // issue the cp.async loads of chunk ch into stage ch % S
     auto issue = [&](int ch) {
       unsigned char* st = smem + (ch % S) * stage_bytes;
-      const int k0 = ch * kBK;
-      constexpr int CPR = kBK / 8;  // 16-byte pieces per row
+      const int k0 = ch * BK;
+      constexpr int CPR = BK / 8;  // 16-byte pieces per row
       for (int e = tid; e < NW * kBT * CPR; e += 512) {
         const int rw = e / CPR, pc = e - rw * CPR;
         const int w = rw / kBT, row = rw - w * kBT;

@@ -374,15 +374,23 @@ pi_status launch_batched(const pi_ffn_desc& D, const pi_layer_weights& w, const 
   if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
   // phase 1
   const int nw = D.gated ? 2 : 1;
-  const int smem1 = kBStages * ((nw * kBT + 2 * a.bp) * kRowB) + 8 * 32 * 4 * nw * 4;
+  // plain layers take 256-column chunks when d allows (fewer pipeline steps
+  // per byte); gated ones 128 (their stages would not fit three deep)
+  const bool wide = !D.gated && D.d % 256 == 0;
+  const int rowb = (wide ? 256 : 128) * 2 + 16;
+  const int smem1 = kBStages * ((nw * kBT + 2 * a.bp) * rowb) + 8 * 32 * 4 * nw * 4;
   using Fn = void (*)(const BatchArgs);
   Fn f1;
   if (!bf) {
-    if (!D.gated) f1 = m2 ? bup_kernel<0, false, 2> : bup_kernel<0, false, 1>;
-    else f1 = m2 ? bup_kernel<0, true, 2> : bup_kernel<0, true, 1>;
+    if (!D.gated)
+      f1 = wide ? (m2 ? bup_kernel<0, false, 2, 256> : bup_kernel<0, false, 1, 256>)
+                : (m2 ? bup_kernel<0, false, 2, 128> : bup_kernel<0, false, 1, 128>);
+    else f1 = m2 ? bup_kernel<0, true, 2, 128> : bup_kernel<0, true, 1, 128>;
   } else {
-    if (!D.gated) f1 = m2 ? bup_kernel<1, false, 2> : bup_kernel<1, false, 1>;
-    else f1 = m2 ? bup_kernel<1, true, 2> : bup_kernel<1, true, 1>;
+    if (!D.gated)
+      f1 = wide ? (m2 ? bup_kernel<1, false, 2, 256> : bup_kernel<1, false, 1, 256>)
+                : (m2 ? bup_kernel<1, false, 2, 128> : bup_kernel<1, false, 1, 128>);
+    else f1 = m2 ? bup_kernel<1, true, 2, 128> : bup_kernel<1, true, 1, 128>;
   }
   if (smem1 + 1024 > di.smem_optin) return PI_ERR_SHAPE;
   s = ensure_smem(reinterpret_cast<const void*>(f1), smem1);
