@@ -204,11 +204,11 @@ __global__ void __launch_bounds__(256) blogit_kernel(const uint16_t* A, const fl
   cp_async_commit();
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
-  float acc[MT][4];
+  float acc[MT][4], accl[MT][4];  // products of the high / low parts (independent chains)
 #pragma unroll
   for (int m = 0; m < MT; ++m)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) acc[m][e] = 0.f;
+    for (int e = 0; e < 4; ++e) acc[m][e] = accl[m][e] = 0.f;
   for (int ks = 0; ks < (r >> 4); ++ks) {
     uint32_t b[2];
     ldsm_x2(b, As + (size_t)(warp * 8 + (lane & 7)) * rowb + (ks * 16 + 8 * ((lane >> 3) & 1)) * 2);
@@ -220,9 +220,13 @@ __global__ void __launch_bounds__(256) blogit_kernel(const uint16_t* A, const fl
       ldsm_x4(ah, Us + (size_t)rr * rowb + cb);
       ldsm_x4(al, Us + (size_t)(bp + rr) * rowb + cb);
       mma16816<DT>(acc[m], ah, b);
-      mma16816<DT>(acc[m], al, b);
+      mma16816<DT>(accl[m], al, b);
     }
   }
+#pragma unroll
+  for (int m = 0; m < MT; ++m)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[m][e] += accl[m][e];
   const int g = lane >> 2, tq = lane & 3;
 #pragma unroll
   for (int m = 0; m < MT; ++m)
@@ -310,11 +314,11 @@ __global__ void __launch_bounds__(512, 1) bup_kernel(const BatchArgs a) {
         cp_async16(xs_ + (size_t)rw * kRowB + 16 * pc, src);
       }
     };
-    float acc[NW][4];
+    float acc[NW][4], accl[NW][4];  // products of the high / low parts (independent chains)
 #pragma unroll
     for (int w = 0; w < NW; ++w)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[w][e] = 0.f;
+      for (int e = 0; e < 4; ++e) acc[w][e] = accl[w][e] = 0.f;
     for (int ch = 0; ch < S - 1; ++ch) {  // always S - 1 groups
       if (ch < nchunks) issue(ch);
       cp_async_commit();
@@ -343,11 +347,15 @@ __global__ void __launch_bounds__(512, 1) bup_kernel(const BatchArgs a) {
           const int cbyte = (ks * 16 + 8 * ((lane >> 3) & 1)) * 2;
           ldsm_x2(b, st + (size_t)r * kRowB + cbyte);
           mma16816<DT>(acc[w], ah, b);
-          mma16816<DT>(acc[w], al, b);
+          mma16816<DT>(accl[w], al, b);
         }
       }
       __syncthreads();
     }
+#pragma unroll
+    for (int w = 0; w < NW; ++w)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[w][e] += accl[w][e];
     // MT = 1: the two k-parity halves meet (fixed order: even + odd)
     if (MT == 1) {
       if (kpar == 1) {
@@ -419,13 +427,13 @@ __global__ void __launch_bounds__(512, 1) bdown_kernel(const BatchArgs a) {
   const uint16_t* w2base = a.W2;
   // warp w owns n tiles w, w + 16, w + 32 (< NT), all m tiles
   constexpr int NTW = 3;
-  float acc[NTW][MT][4];
+  float acc[NTW][MT][4], accl[NTW][MT][4];  // high / low part products (independent chains)
 #pragma unroll
   for (int q = 0; q < NTW; ++q)
 #pragma unroll
     for (int m = 0; m < MT; ++m)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[q][m][e] = 0.f;
+      for (int e = 0; e < 4; ++e) acc[q][m][e] = accl[q][m][e] = 0.f;
   const int nchunks = (hi_u - lo_u + kBN2 - 1) / kBN2;
   auto issue = [&](int ch) {
     unsigned char* st = smem + (ch % S) * stage_bytes;
@@ -501,7 +509,7 @@ __global__ void __launch_bounds__(512, 1) bdown_kernel(const BatchArgs a) {
 #pragma unroll
           for (int m = 0; m < MT; ++m) {
             mma16816<DT>(acc[q][m], ah[m], b);
-            mma16816<DT>(acc[q][m], al[m], b);
+            mma16816<DT>(accl[q][m], al[m], b);
           }
         }
       }
@@ -520,7 +528,7 @@ __global__ void __launch_bounds__(512, 1) bdown_kernel(const BatchArgs a) {
         for (int e = 0; e < 4; ++e) {
           const int t = m * 16 + gq + 8 * (e >> 1);
           const int col = c0 + ntile * 8 + 2 * tq + (e & 1);
-          a.part[((size_t)g * a.bp + t) * a.d + col] = acc[q][m][e];
+          a.part[((size_t)g * a.bp + t) * a.d + col] = acc[q][m][e] + accl[q][m][e];
         }
     }
   }
