@@ -459,7 +459,10 @@ def run_ours(args):
             "workload": args.workload, "batch": 1, "weights": w["dtype"], "density": w["density"],
             "d": d, "n": n, "r": r, "gated": gated, "hot_prefix": hot, "layout": args.layout,
             "l2": (f"inputs larger than L2: {R} rotating weight replicas "
-                   f"({R * layer_bytes / 1e9:.1f} GB; each step reads its own copy)"),
+                   f"({R * layer_bytes / 1e9:.1f} GB; each step reads its own copy)"
+                   if R * step_bytes_est >= 3 * l2 else
+                   f"L2-warm (not HBM-bound): {R} weight replica(s) of "
+                   f"{layer_bytes / 1e9:.2f} GB reused across steps"),
             "graph_len": G, "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "us_per_layer": ms_per_step * 1e3,
@@ -476,7 +479,9 @@ def run_ours(args):
                       "frac": dense_bytes / (dense_ms / 1e3) / 1e9 / peak},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": d * 4,
                 "d2h_bytes_per_step": d * 4, "steps": e2e_done,
-                "how": "CUDA-graph replay of (pinned H2D x, pi_layer_decode, D2H y) per step"},
+                "how": (f"CUDA-graph replay per {G} steps of (pinned H2D of their x, one "
+                        f"pi_decode_layers launch, D2H of their y)" if seq else
+                        "CUDA-graph replay of (pinned H2D x, pi_layer_decode, D2H y) per step")},
         "gpu_launches": launches,
         "engine": args.engine,
         "clocks": clocks,
