@@ -277,15 +277,15 @@ __global__ void __launch_bounds__(512, 1) bup_kernel(const BatchArgs a) {
   const int hi_u = (int)((long long)(blockIdx.x + 1) * U / a.P);
   const int stage_bytes = bup_stage_bytes<GATED, BK>(a.bp);
   constexpr int NW = GATED ? 2 : 1;
-  // warp -> (m tile, n tile, k parity): MT = 2: 16 fragments, one per warp;
-  // MT = 1: 8 fragments, two warps each, taking alternate k-steps.
-  const int nt = warp & 7;
-  const int mt = (MT == 2) ? (warp >> 3) : 0;
-  const int kpar = (MT == 2) ? 0 : (warp >> 3);
+  // warp -> (n group: n tiles 2 ng and 2 ng + 1; k quarter: k-steps
+  // kq, kq + 4, ...), every m tile: one x fragment feeds 2 NW products per
+  // part, the B fragments of both n tiles come in one ldmatrix.x4
+  const int ng = warp & 3, kq = warp >> 2;
   const int ksteps = BK / 16;
   const int nchunks = a.d / BK;
   constexpr int S = kBStages;
-  float* comb = reinterpret_cast<float*>(smem + S * stage_bytes);  // [8][32][4 * NW]
+  constexpr int CV = NW * MT * 2 * 4;  // accumulator values per lane
+  float* comb = reinterpret_cast<float*>(smem + S * stage_bytes);  // [3][4][32][CV]
   const size_t w1s = a.packed ? (size_t)a.rec : (GATED ? 2 * (size_t)a.d : (size_t)a.d);
 
   for (int t0 = lo_u; t0 < hi_u; t0 += kBT) {
@@ -314,11 +314,16 @@ __global__ void __launch_bounds__(512, 1) bup_kernel(const BatchArgs a) {
         cp_async16(xs_ + (size_t)rw * kRowB + 16 * pc, src);
       }
     };
-    float acc[NW][4], accl[NW][4];  // products of the high / low parts (independent chains)
+    // products of the high / low parts (independent chains), [w][m][n tile][e]
+    float acc[NW][MT][2][4], accl[NW][MT][2][4];
 #pragma unroll
     for (int w = 0; w < NW; ++w)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[w][e] = accl[w][e] = 0.f;
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[w][m][j][e] = accl[w][m][j][e] = 0.f;
     for (int ch = 0; ch < S - 1; ++ch) {  // always S - 1 groups
       if (ch < nchunks) issue(ch);
       cp_async_commit();
@@ -330,68 +335,82 @@ __global__ void __launch_bounds__(512, 1) bup_kernel(const BatchArgs a) {
       __syncthreads();
       const unsigned char* st = smem + (ch % S) * stage_bytes;
       const unsigned char* xs_ = st + (size_t)NW * kBT * kRowB;
-      for (int ks = kpar; ks < ksteps; ks += (MT == 2 ? 1 : 2)) {
-        uint32_t ah[4], al[4];
-        {
-          // A fragment rows: tokens mt*16 .. +15, columns ks*16 .. +15
-          const int r = mt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+      for (int ks = kq; ks < ksteps; ks += 4) {
+        uint32_t ah[MT][4], al[MT][4];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          // A fragment rows: tokens m*16 .. +15, columns ks*16 .. +15
+          const int r = m * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
           const int cbyte = (ks * 16 + 8 * (lane >> 4)) * 2;
-          ldsm_x4(ah, xs_ + (size_t)r * kRowB + cbyte);
-          ldsm_x4(al, xs_ + (size_t)(a.bp + r) * kRowB + cbyte);
+          ldsm_x4(ah[m], xs_ + (size_t)r * kRowB + cbyte);
+          ldsm_x4(al[m], xs_ + (size_t)(a.bp + r) * kRowB + cbyte);
         }
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
-          uint32_t b[2];
-          // B fragment: neurons nt*8 .. +7 (rows), k = ks*16 .. +15
-          const int r = w * kBT + nt * 8 + (lane & 7);
+          // B fragments of n tiles 2 ng (b4[0..1]) and 2 ng + 1 (b4[2..3]):
+          // neurons ng*16 .. +15 (rows), k = ks*16 .. +15
+          uint32_t b4[4];
+          const int r = w * kBT + ng * 16 + (lane & 7) + 8 * (lane >> 4);
           const int cbyte = (ks * 16 + 8 * ((lane >> 3) & 1)) * 2;
-          ldsm_x2(b, st + (size_t)r * kRowB + cbyte);
-          mma16816<DT>(acc[w], ah, b);
-          mma16816<DT>(accl[w], al, b);
+          ldsm_x4(b4, st + (size_t)r * kRowB + cbyte);
+          const uint32_t b0[2] = {b4[0], b4[1]}, b1[2] = {b4[2], b4[3]};
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            mma16816<DT>(acc[w][m][0], ah[m], b0);
+            mma16816<DT>(accl[w][m][0], al[m], b0);
+            mma16816<DT>(acc[w][m][1], ah[m], b1);
+            mma16816<DT>(accl[w][m][1], al[m], b1);
+          }
         }
       }
       __syncthreads();
     }
+    // high + low, then the four k quarters meet in a fixed order (0, 1, 2, 3)
+    float v[CV];
 #pragma unroll
     for (int w = 0; w < NW; ++w)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[w][e] += accl[w][e];
-    // MT = 1: the two k-parity halves meet (fixed order: even + odd)
-    if (MT == 1) {
-      if (kpar == 1) {
+      for (int m = 0; m < MT; ++m)
 #pragma unroll
-        for (int w = 0; w < NW; ++w)
+        for (int jn = 0; jn < 2; ++jn)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) comb[(nt * 32 + lane) * 4 * NW + w * 4 + e] = acc[w][e];
-      }
-      __syncthreads();
-      if (kpar == 0) {
+          for (int e = 0; e < 4; ++e)
+            v[((w * MT + m) * 2 + jn) * 4 + e] = acc[w][m][jn][e] + accl[w][m][jn][e];
+    if (kq > 0) {
+      float* cp = comb + ((size_t)((kq - 1) * 4 + ng) * 32 + lane) * CV;
 #pragma unroll
-        for (int w = 0; w < NW; ++w)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[w][e] += comb[(nt * 32 + lane) * 4 * NW + w * 4 + e];
-      }
+      for (int e = 0; e < CV; ++e) cp[e] = v[e];
     }
-    // epilogue: bias, activation, the token's own mask bit, split, store H^T
-    if (MT == 2 || kpar == 0) {
+    __syncthreads();
+    if (kq == 0) {
+      for (int q = 1; q < 4; ++q) {
+        const float* cp = comb + ((size_t)((q - 1) * 4 + ng) * 32 + lane) * CV;
+#pragma unroll
+        for (int e = 0; e < CV; ++e) v[e] += cp[e];
+      }
+      // epilogue: bias, activation, the token's own mask bit, split, store H^T
       const int g = lane >> 2, tq = lane & 3;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int t = mt * 16 + g + 8 * (e >> 1);      // token (row of the fragment)
-        const int col = nt * 8 + 2 * tq + (e & 1);     // neuron within the tile
-        if (col < tn && t < a.batch) {
-          const int pos = t0 + col;
-          const int nid = a.dense ? pos : __ldg(a.uidx + pos);
-          float h = acc[0][e] + __ldg(a.b1 + nid);
-          h = h > 0.f ? h : 0.f;  // ReLU; ReLU(0) = 0
-          if (GATED) h *= acc[NW - 1][e];
-          if (!a.dense && !((__ldg(a.tmask + pos) >> t) & 1u)) h = 0.f;  // token t skips it
-          uint16_t hh, hl;
-          split16<DT>(h, &hh, &hl);
-          a.hhi[(size_t)t * a.hs + pos] = hh;
-          a.hlo[(size_t)t * a.hs + pos] = hl;
-        }
-      }
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int jn = 0; jn < 2; ++jn)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int t = m * 16 + g + 8 * (e >> 1);                 // token
+            const int col = (2 * ng + jn) * 8 + 2 * tq + (e & 1);    // neuron within the tile
+            if (col < tn && t < a.batch) {
+              const int pos = t0 + col;
+              const int nid = a.dense ? pos : __ldg(a.uidx + pos);
+              float h = v[((0 * MT + m) * 2 + jn) * 4 + e] + __ldg(a.b1 + nid);
+              h = h > 0.f ? h : 0.f;  // ReLU; ReLU(0) = 0
+              if (GATED) h *= v[(((NW - 1) * MT + m) * 2 + jn) * 4 + e];
+              if (!a.dense && !((__ldg(a.tmask + pos) >> t) & 1u)) h = 0.f;  // token t skips it
+              uint16_t hh, hl;
+              split16<DT>(h, &hh, &hl);
+              a.hhi[(size_t)t * a.hs + pos] = hh;
+              a.hlo[(size_t)t * a.hs + pos] = hl;
+            }
+          }
     }
     __syncthreads();
   }
