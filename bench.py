@@ -53,6 +53,19 @@ def aggregate(per_rank_ms, per_rank_units, n_gpus):
     return (sum(per_rank_units) / (t / 1e3)) if t > 0 else 0.0, t
 
 
+def max_over_ranks(value: float, world: int, device="cpu") -> float:
+    """The largest of every rank's value (one all-reduce; the value itself
+    when there is one rank).  device: where the reduction's tensor lives
+    (the rank's GPU under NCCL, the CPU under gloo)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def csrc_hash():
     h = hashlib.sha256()
     d = os.path.join(ROOT, "activation_sparse_decode_rank_gb300", "csrc")
@@ -352,13 +365,7 @@ def run_ours(args):
     alg_bytes = pred_bytes + active_bytes
 
     # max over ranks
-    ms_all = [ms]
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_all = [float(tt.item())]
-    value, t_max = aggregate(ms_all, [args.steps * world], world)
+    value, t_max = aggregate([max_over_ranks(ms, world, dev)], [args.steps * world], world)
     ms_per_step = t_max / args.steps
     launches = args.steps // steps_per_call
     per_launch_s = ms / launches / 1e3
@@ -426,13 +433,7 @@ def run_ours(args):
     stream.synchronize()
     e2e_ms = f0.elapsed_time(f1)
     e2e_done = full * G
-    e2e_ms_all = [e2e_ms]
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms_all = [float(tt.item())]
-    e2e_value, _ = aggregate(e2e_ms_all, [e2e_done * world], world)
+    e2e_value, _ = aggregate([max_over_ranks(e2e_ms, world, dev)], [e2e_done * world], world)
 
     if rank != 0:
         if world > 1:
