@@ -65,6 +65,11 @@ __device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], const void* p) {
                : "=r"(r[0]), "=r"(r[1])
                : "r"(smem_u32(p)));
 }
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
 __device__ __forceinline__ void ldsm_x2_t(uint32_t (&r)[2], const void* p) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
                : "=r"(r[0]), "=r"(r[1])
@@ -444,15 +449,19 @@ __global__ void __launch_bounds__(512, 1) bdown_kernel(const BatchArgs a) {
   constexpr int S = kBStages;
   const size_t w2s = a.packed ? (size_t)a.rec : (size_t)a.d;  // W2 rows (packed: inside records)
   const uint16_t* w2base = a.W2;
-  // warp w owns n tiles w, w + 16, w + 32 (< NT), all m tiles
-  constexpr int NTW = 3;
-  float acc[NTW][MT][4], accl[NTW][MT][4];  // high / low part products (independent chains)
+  // warp w owns the n-tile pairs w and w + 16 (tiles 2p, 2p + 1 < NT), all
+  // m tiles; one ldmatrix.x4.trans loads the B fragments of a pair
+  constexpr int NPW = 2;
+  // high / low part products (independent chains), [pair][tile][m][e]
+  float acc[NPW][2][MT][4], accl[NPW][2][MT][4];
 #pragma unroll
-  for (int q = 0; q < NTW; ++q)
+  for (int q = 0; q < NPW; ++q)
 #pragma unroll
-    for (int m = 0; m < MT; ++m)
+    for (int j = 0; j < 2; ++j)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[q][m][e] = accl[q][m][e] = 0.f;
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[q][j][m][e] = accl[q][j][m][e] = 0.f;
   const int nchunks = (hi_u - lo_u + kBN2 - 1) / kBN2;
   auto issue = [&](int ch) {
     unsigned char* st = smem + (ch % S) * stage_bytes;
@@ -517,18 +526,22 @@ __global__ void __launch_bounds__(512, 1) bdown_kernel(const BatchArgs a) {
         ldsm_x4(al[m], hs_ + (size_t)(a.bp + r) * kHRowB + cbyte);
       }
 #pragma unroll
-      for (int q = 0; q < NTW; ++q) {
-        const int ntile = warp + 16 * q;
-        if (ntile < NT) {
-          uint32_t b[2];
-          // W2 stored [k = neuron][n = column]: transposed load gives the
-          // (k pair, n) layout of the B operand
+      for (int q = 0; q < NPW; ++q) {
+        const int pr = warp + 16 * q;
+        if (2 * pr < NT) {
+          // W2 stored [k = neuron][n = column]: transposed loads give the
+          // (k pair, n) layout of the B operand; matrices 0/1: tile 2 pr,
+          // 2/3: tile 2 pr + 1 (within the padded row even past NT)
+          uint32_t b4[4];
           const int kr = ks * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
-          ldsm_x2_t(b, st + (size_t)kr * w2row + ntile * 16);
+          ldsm_x4_t(b4, st + (size_t)kr * w2row + (2 * pr + (lane >> 4)) * 16);
+          const uint32_t b0[2] = {b4[0], b4[1]}, b1[2] = {b4[2], b4[3]};
 #pragma unroll
           for (int m = 0; m < MT; ++m) {
-            mma16816<DT>(acc[q][m], ah[m], b);
-            mma16816<DT>(accl[q][m], al[m], b);
+            mma16816<DT>(acc[q][0][m], ah[m], b0);
+            mma16816<DT>(accl[q][0][m], al[m], b0);
+            mma16816<DT>(acc[q][1][m], ah[m], b1);
+            mma16816<DT>(accl[q][1][m], al[m], b1);
           }
         }
       }
@@ -538,19 +551,21 @@ __global__ void __launch_bounds__(512, 1) bdown_kernel(const BatchArgs a) {
   // partial Y of group g, this slice
   const int gq = lane >> 2, tq = lane & 3;
 #pragma unroll
-  for (int q = 0; q < NTW; ++q) {
-    const int ntile = warp + 16 * q;
-    if (ntile < NT) {
+  for (int q = 0; q < NPW; ++q)
 #pragma unroll
-      for (int m = 0; m < MT; ++m)
+    for (int j = 0; j < 2; ++j) {
+      const int ntile = 2 * (warp + 16 * q) + j;
+      if (ntile < NT) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int t = m * 16 + gq + 8 * (e >> 1);
-          const int col = c0 + ntile * 8 + 2 * tq + (e & 1);
-          a.part[((size_t)g * a.bp + t) * a.d + col] = acc[q][m][e] + accl[q][m][e];
-        }
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int t = m * 16 + gq + 8 * (e >> 1);
+            const int col = c0 + ntile * 8 + 2 * tq + (e & 1);
+            a.part[((size_t)g * a.bp + t) * a.d + col] = acc[q][j][m][e] + accl[q][j][m][e];
+          }
+      }
     }
-  }
 }
 
 // ---------------------------------------------------------------- phase 3

@@ -346,7 +346,7 @@ pi_status launch_batched(const pi_ffn_desc& D, const pi_layer_weights& w, const 
   a.bp = L.bp;
   a.P = di.sms;
   a.slices = di.sms / kGroups2 > 0 ? di.sms / kGroups2 : 1;
-  a.cw = (int)round_up((size_t)((D.d + a.slices - 1) / a.slices), 8);
+  a.cw = (int)round_up((size_t)((D.d + a.slices - 1) / a.slices), 16);  // whole n-tile pairs
   a.packed = D.layout == PI_LAYOUT_PACKED;
   a.rec = (D.gated ? 3 : 2) * D.d;
   a.W1 = static_cast<const uint16_t*>(w.W1);
@@ -402,7 +402,7 @@ pi_status launch_batched(const pi_ffn_desc& D, const pi_layer_weights& w, const 
   const int smem2 = kBStages * bdn_stage_bytes(a.cw, a.bp);
   Fn f2 = bf ? (m2 ? bdown_kernel<1, 2> : bdown_kernel<1, 1>)
              : (m2 ? bdown_kernel<0, 2> : bdown_kernel<0, 1>);
-  if (smem2 + 1024 > di.smem_optin || a.cw / 8 > 48) return PI_ERR_SHAPE;
+  if (smem2 + 1024 > di.smem_optin || a.cw / 8 > 64) return PI_ERR_SHAPE;
   s = ensure_smem(reinterpret_cast<const void*>(f2), smem2);
   if (s != PI_OK) return s;
   f2<<<kGroups2 * a.slices, 512, smem2, st>>>(a);
