@@ -44,6 +44,8 @@ struct BatchArgs {
   const int* uidx;            // union neurons, ascending
   const int* ucnt;            // union count (device)
   int dense;                  // 1: all n neurons, every token (uidx / ucnt / tmask unused)
+  int tc_cols;                // tensor-memory columns of the tcgen05 phase 1
+  unsigned long long limit_ns;  // bound of every wait (tcgen05 phase 1)
   const uint32_t* tmask;      // token bitmask per union position
   uint16_t* xhi;              // [bp][d] activations, high and low 16-bit parts
   uint16_t* xlo;

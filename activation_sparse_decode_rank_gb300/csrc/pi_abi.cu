@@ -11,6 +11,7 @@
 #include "kernels.cuh"
 #include "batched.cuh"
 #include "seq.cuh"
+#include "tc.cuh"
 
 using namespace pik;
 
@@ -334,7 +335,7 @@ void bind_weights(FfnArgs& a, const pi_layer_weights& w) {
 pi_status launch_batched(const pi_ffn_desc& D, const pi_layer_weights& w, const float* x,
                          int batch, const int* uidx, const int* ucnt, const uint32_t* tmask,
                          float* y, const float* residual, const WsLayout& L, void* ws,
-                         cudaStream_t st) {
+                         cudaStream_t st, int32_t* dev_status) {
   DevInfo di;
   pi_status s = dev_info(&di);
   if (s != PI_OK) return s;
@@ -366,6 +367,7 @@ pi_status launch_batched(const pi_ffn_desc& D, const pi_layer_weights& w, const 
   a.hlo = reinterpret_cast<uint16_t*>(b + L.hlo);
   a.hs = L.hs;
   a.part = reinterpret_cast<float*>(b + L.bpart);
+  a.status = dev_status;  // may be NULL
   const bool bf = D.dtype == PI_BF16;
   const bool m2 = a.bp == 32;
   // phase 0: split x
@@ -393,10 +395,27 @@ pi_status launch_batched(const pi_ffn_desc& D, const pi_layer_weights& w, const 
                 : (m2 ? bup_kernel<1, false, 2, 128> : bup_kernel<1, false, 1, 128>);
     else f1 = m2 ? bup_kernel<1, true, 2, 128> : bup_kernel<1, true, 1, 128>;
   }
-  if (smem1 + 1024 > di.smem_optin) return PI_ERR_SHAPE;
-  s = ensure_smem(reinterpret_cast<const void*>(f1), smem1);
+  int smem_launch = smem1;
+  // tcgen05 phase 1 with PI_BATCH_TC=1 (measured slower than the mma.sync
+  // kernel so far: one commit round trip per 64-128-column chunk)
+  bool use_tc = false;
+  if (const char* e = std::getenv("PI_BATCH_TC")) use_tc = std::atoi(e) != 0;
+  if (use_tc) {
+    const int mh = 1;  // 128-position tiles (measured faster than 256 with narrower chunks)
+    int cols = mh * nw * a.bp, pw = 32;
+    while (pw < cols) pw <<= 1;
+    a.tc_cols = pw;
+    const int stg = kTcStages * (D.gated ? tc_stage_bytes<true, 1>(a.bp)
+                                         : tc_stage_bytes<false, 1>(a.bp));
+    if (!bf) f1 = D.gated ? bup_tc_kernel<0, true, 1> : bup_tc_kernel<0, false, 1>;
+    else f1 = D.gated ? bup_tc_kernel<1, true, 1> : bup_tc_kernel<1, false, 1>;
+    smem_launch = stg;
+    a.limit_ns = wait_limit_ns();
+  }
+  if (smem_launch + 1024 > di.smem_optin) return PI_ERR_SHAPE;
+  s = ensure_smem(reinterpret_cast<const void*>(f1), smem_launch);
   if (s != PI_OK) return s;
-  f1<<<a.P, 512, smem1, st>>>(a);
+  f1<<<a.P, 512, smem_launch, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
   // phase 2
   const int smem2 = kBStages * bdn_stage_bytes(a.cw, a.bp);
@@ -674,9 +693,8 @@ pi_status pi_sparse_ffn(const pi_ffn_desc* desc, const pi_layer_weights* w, cons
     (void)idx;
     (void)cnt;
     (void)cap;
-    (void)dev_status;
     return launch_batched(*desc, *w, x, batch, union_idx, union_cnt, tok_mask, y, nullptr, L, ws,
-                          reinterpret_cast<cudaStream_t>(stream));
+                          reinterpret_cast<cudaStream_t>(stream), dev_status);
   }
   if (!x || !y || !idx || !cnt || !dev_status || !ws) return PI_ERR_NULL;
   const void* ps[] = {x, y, idx, cnt, dev_status, ws};
@@ -715,7 +733,7 @@ pi_status pi_dense_ffn(const pi_ffn_desc* desc, const pi_layer_weights* w, const
   if (ws_bytes < L.total) return PI_ERR_WORKSPACE;
   if (batch > 1 && desc->d % kBK == 0)  // every row read once for all tokens, tensor cores
     return launch_batched(*desc, *w, x, batch, nullptr, nullptr, nullptr, y, nullptr, L, ws,
-                          reinterpret_cast<cudaStream_t>(stream));
+                          reinterpret_cast<cudaStream_t>(stream), nullptr);
   for (int t = 0; t < batch; ++t) {
     FfnArgs a{};
     bind_weights(a, *w);
@@ -762,7 +780,7 @@ pi_status pi_layer_decode(const pi_ffn_desc* desc, const pi_layer_weights* w, co
                    ws_bytes, stream);
     if (s != PI_OK) return s;
     return launch_batched(*desc, *w, x, batch, uidx, ucnt, tmask, y, residual, L, ws,
-                          reinterpret_cast<cudaStream_t>(stream));
+                          reinterpret_cast<cudaStream_t>(stream), dev_status);
   }
   for (int t = 0; t < batch; ++t) {
     FfnArgs a{};

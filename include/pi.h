@@ -164,10 +164,13 @@ pi_status pi_compact(const float* logits, int32_t n, int32_t batch,
  * written to *dev_status.
  * batch > 1: the union form; union_idx / union_cnt / tok_mask as written by
  * pi_compact, and token t uses exactly the union neurons whose mask bit t is
- * set, so y[t] equals the batch-1 result for token t (idx, cnt, cap and
- * dev_status are then unused).  The union's rows are read once and
- * contracted with all tokens on the tensor cores (16-bit operands with a
- * high/low split of x and h, fp32 accumulation); needs d % 128 == 0. */
+ * set, so y[t] equals the batch-1 result for token t (idx, cnt and cap are
+ * then unused; dev_status, if not NULL, receives PI_ERR_TIMEOUT should a
+ * bounded wait of the tensor-core phase run out).  The union's rows are
+ * read once and contracted with all tokens on the tensor cores (16-bit
+ * operands with a high/low split of x and h, fp32 accumulation; the
+ * environment variable PI_BATCH_TC=1 selects a tcgen05 up projection with
+ * its accumulator in tensor memory); needs d % 128 == 0. */
 pi_status pi_sparse_ffn(const pi_ffn_desc* desc, const pi_layer_weights* w,
                         const float* x, int32_t batch, const int32_t* idx,
                         const int32_t* cnt, int32_t cap,

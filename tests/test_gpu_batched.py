@@ -167,3 +167,28 @@ def test_dense_batched_gated_full_size():
         for t in (0, 3):
             yd = oracle.dense_ffn(D.L, x[t])
             assert float(np.abs(yh[t] - yd).max()) / float(np.abs(yd).max()) <= Y_TOL
+
+
+@pytest.mark.parametrize("gated", [False, True])
+def test_tcgen05_up_projection(gated, monkeypatch):
+    """The tcgen05 up projection (PI_BATCH_TC=1) under the same rules."""
+    monkeypatch.setenv("PI_BATCH_TC", "1")
+    if gated:
+        D = dev_layer("llama", lambda: synth.make_layer(4096, 11008, 256, "bf16", gated=True,
+                                                         alpha=1.0, density=0.10, seed=3))
+        x = synth.gen_x(70, 0, 5, 4096)
+        tokens = [0, 4]
+    else:
+        D = opt13b(0.10)
+        x = synth.gen_x(71, 0, 32, 5120)
+        tokens = [0, 17, 31]
+    for packed in (False, True):
+        y, idxs, st = decode_batch(D, x, packed=packed)
+        assert st == 0
+        check_tokens(D.L, x, y, idxs, tokens=tokens)
+    yd = torch.empty((x.shape[0], D.L.d), device=DEV)
+    pi.check(pi.pi_dense_ffn(D.desc, D.w, up(x, DEV), x.shape[0], yd, D.workspace(x.shape[0])))
+    torch.cuda.synchronize()
+    for t in tokens:
+        want = oracle.dense_ffn(D.L, x[t])
+        assert float(np.abs(yd.cpu().numpy()[t] - want).max()) <= Y_TOL * float(np.abs(want).max())
