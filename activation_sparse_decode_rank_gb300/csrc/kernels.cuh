@@ -68,6 +68,10 @@ __device__ __forceinline__ void cp_async4(void* sdst, const void* gsrc) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // Bulk prefetch of [p, p + bytes) into L2 (TMA unit; no completion to wait on).
 __device__ __forceinline__ void prefetch_l2(const void* p, unsigned long long bytes) {

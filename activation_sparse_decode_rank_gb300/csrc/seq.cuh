@@ -22,11 +22,12 @@
 //   L  full x and u, logits of the block's own neurons, their ordered
 //      active list;
 //      ring: the row-gather GEMV + ReLU and row-axpy of those neurons;
-//      then the next job's weights that do not depend on its x (the own hot
-//      neurons' rows into ring slots, the rest of the hot rows and the
-//      predictor rows towards L2 / shared memory) are requested, so that
-//      their transfer overlaps this job's tail;
 //   -- wait 2 -- (partial rows written)
+// Right after wait 2, the warps that R leaves idle request the next job's
+// weights that do not depend on its x (the own hot neurons' rows into ring
+// slots, its Bm columns and predictor rows into shared memory, the rest
+// towards L2), so that their transfer overlaps R, U and wait 1 instead of
+// delaying this block's arrival at wait 2.
 // With balancing on (large layers), the blocks publish their cold active
 // neurons after the lists are built and, after one more grid-wide wait, each
 // takes an equal share of them by global rank.
@@ -98,10 +99,16 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
   const int rc = f.r >> 3;
   int nh_c = 0;   // own hot neurons whose rows went to slots for the current job
 
-  // Requests the weights of job j that do not depend on its x.  No copy may
-  // be in flight (the ring barriers are re-armed).
+  // The weights of job j that do not depend on its x.  prep_set points the
+  // job's arguments at them; prep_issue requests them: the producer lane
+  // re-arms the ring barriers (no copy may be in flight) and sends the own hot
+  // neurons' rows to their slots; compute threads [t0, t0 + nt) stage the own
+  // Bm columns ([k][q], 16 bytes each, in the last ring slot, a cold one) as
+  // one copy group, then the predictor rows and biases (or prefetch them and
+  // the hot rows beyond the slots towards L2) as a second group, so that
+  // stage 1 waits for the first group only.
   bool armed = false;  // the ring barriers hold a previous job's state
-  auto prep = [&](int j) {
+  auto prep_set = [&](int j) {
     const SeqLayer& Lw = sa.L[j % sa.R];
     a.A = Lw.A;
     a.Bm = Lw.Bm;
@@ -110,9 +117,10 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
     a.W2 = Lw.W2;
     a.b2 = Lw.b2;
     a.hot = Lw.hot;
-    const int hot_own = (c < a.hot) ? (a.hot - 1 - c) / P + 1 : 0;
-    nh_c = min(f.nh, hot_own);
-    if (tid == 0) {
+    nh_c = min(f.nh, (c < a.hot) ? (a.hot - 1 - c) / P + 1 : 0);
+  };
+  auto prep_issue = [&](int t0, int nt) {
+    if (tid == kThreads) {
       for (int s = 0; s < f.ns; ++s) {
         if (armed) {
           mbar_inval(full + s);
@@ -125,27 +133,27 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
       for (int k = 0; k < nh_c; ++k) issue_neuron<GATED>(a, slots, full, k, c + k * P);
     }
     armed = true;
-    if (compute) {
-      // the own hot neurons beyond the slots and (unless staged) the own
-      // predictor rows towards L2; staged predictor rows, biases and own Bm
-      // columns ([k][q], 16 bytes each, in the last ring slot, a cold one)
-      for (int k = nh_c + tid; k < hot_own; k += kThreads) prefetch_neuron<GATED>(a, c + k * P);
+    const int t = tid - t0;
+    if (t >= 0 && t < nt) {
+      const int hot_own = (c < a.hot) ? (a.hot - 1 - c) / P + 1 : 0;
+      if (sa.bm_smem)
+        for (int e = t; e < f.r * nq; e += nt) {
+          const int k = e / nq, q = e - k * nq;
+          cp_async16(bms + (size_t)e * 16, a.Bm + (size_t)k * f.d + 8 * (q0 + q));
+        }
+      cp_async_commit();
+      for (int k = nh_c + t; k < hot_own; k += nt) prefetch_neuron<GATED>(a, c + k * P);
       if (f.a_in_smem) {
-        for (int e = tid; e < rows * rc; e += kThreads) {
+        for (int e = t; e < rows * rc; e += nt) {
           const int jj = e / rc, q = e - jj * rc;
           cp_async16(As + (size_t)jj * f.a_stride + 16 * q,
                      a.A + ((size_t)c + (size_t)jj * P) * f.r + 8 * q);
         }
       } else {
-        for (int jj = tid; jj < rows; jj += kThreads)
+        for (int jj = t; jj < rows; jj += nt)
           prefetch_l2(a.A + ((size_t)c + (size_t)jj * P) * f.r, (size_t)f.r * 2);
       }
-      if (sa.bm_smem)
-        for (int e = tid; e < f.r * nq; e += kThreads) {
-          const int k = e / nq, q = e - k * nq;
-          cp_async16(bms + (size_t)e * 16, a.Bm + (size_t)k * f.d + 8 * (q0 + q));
-        }
-      for (int jj = tid; jj < rows; jj += kThreads) cp_async4(b1s + jj, a.b1 + c + (size_t)jj * P);
+      for (int jj = t; jj < rows; jj += nt) cp_async4(b1s + jj, a.b1 + c + (size_t)jj * P);
       cp_async_commit();
     }
   };
@@ -158,7 +166,8 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
   };
 
   if (tid == 0) s_bad = 0;
-  prep(0);
+  prep_set(0);
+  prep_issue(0, kThreads);
   pdl_wait();
   if (tid == 0) s_base = grid_base(f.bar, (unsigned)P);
   unsigned long long nbar = 0;
@@ -167,7 +176,7 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
     // own columns of this job's x: job 0 reads them here; later jobs find
     // them in xo (written by the previous job's R phase)
     if (j == 0 && tid < nq * 8) xo[tid] = __ldcg(sa.x + 8 * q0 + tid);
-    cp_async_wait_all();  // this job's staged weights
+    cp_async_wait_group<1>();  // this job's staged Bm columns
     __syncthreads();
     // U: partial predictor stage 1 over the own columns, u_c[k] for k < r
     if (tid < f.r) {
@@ -217,7 +226,7 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
       us[tid] = (float)((double)(long long)v * 2.3283064365386963e-10);  // x 2^-32
       if (c == 0) sa.uacc[((size_t)((j + 1) & 1) * f.r + tid) * 16] = 0ull;
     }
-    cp_async_wait_all();
+    cp_async_wait_all();  // this job's staged predictor rows and biases
     __syncthreads();
     if (compute) own_logits<DT>(a, As, b1s, us, flag, rows);
     __syncthreads();
@@ -342,6 +351,7 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
         if (!used && !mbar_wait(full + k, 0u, f.limit_ns)) set_status(f.status, PI_ERR_TIMEOUT);
       }
     }
+    nh_c = 0;  // every slot copy of this job has landed
     __syncthreads();
     const float* b2j = a.b2;
     if (compute) {  // the partial rows go out first: wait 2 fences them
@@ -355,7 +365,6 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
         }
       }
     }
-    if (j + 1 < sa.J) prep(j + 1);  // overlaps wait 2 and R
     ++nbar;
     if (!grid_sync(f.bar, s_base + nbar * P, f.status, f.limit_ns)) {
       bail();
@@ -418,6 +427,14 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
         }
         reinterpret_cast<float4*>(sa.y + (size_t)j * f.d)[col4] = s;
       }
+    }
+    // The next job's weights: the warps past the 2 nq reducing ones arrive
+    // here at once and request them while R runs (no barrier since wait 2);
+    // if every compute warp reduces, all of them do, after R.
+    if (j + 1 < sa.J) {
+      const int t0 = (nq < kSeqMaxQ) ? 64 * nq : 0;
+      prep_set(j + 1);
+      prep_issue(t0, kThreads - t0);
     }
   }
 }
