@@ -90,7 +90,10 @@ __device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long l
 // Arrival is a fire-and-forget reduction (no round trip); the wait is
 // bounded by limit_ns and records PI_ERR_TIMEOUT when it runs out.  Writes
 // made by the block before the call are visible to every block after it
-// (read them with ld.cg / __ldcg: L1 is not coherent across blocks).
+// (read them with ld.cg / __ldcg: L1 is not coherent across blocks): the
+// block's threads meet at __syncthreads first, and thread 0's release
+// reduction is cumulative over the writes that meeting ordered before it, so
+// no separate fence is needed.
 __device__ __forceinline__ unsigned long long grid_base(const unsigned long long* ctr,
                                                         unsigned nblocks) {
   const unsigned long long v = ld_acquire64(ctr);
@@ -103,7 +106,6 @@ __device__ __noinline__ bool grid_sync(unsigned long long* ctr, unsigned long lo
   __syncthreads();
   if (threadIdx.x == 0) {
     int ok = 1;
-    __threadfence();
     asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(ctr) : "memory");
     const uint64_t t0 = global_ns();
     unsigned spins = 0;
@@ -118,37 +120,6 @@ __device__ __noinline__ bool grid_sync(unsigned long long* ctr, unsigned long lo
   }
   __syncthreads();
   return s_ok != 0;
-}
-
-// The two halves of grid_sync, for work that may run between them (work
-// that touches nothing another block reads).  grid_arrive: every thread of
-// the block calls it after its writes; grid_wait: every thread calls it,
-// the bounded wait of grid_sync.
-__device__ __forceinline__ void grid_arrive(unsigned long long* ctr) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(ctr) : "memory");
-  }
-}
-__device__ __noinline__ bool grid_wait(unsigned long long* ctr, unsigned long long target,
-                                       int* status, uint64_t limit_ns) {
-  __shared__ int s_ok2;
-  if (threadIdx.x == 0) {
-    int ok = 1;
-    const uint64_t t0 = global_ns();
-    unsigned spins = 0;
-    while ((long long)(ld_acquire64(ctr) - target) < 0) {
-      if ((++spins & 15u) == 0u && global_ns() - t0 > limit_ns) {
-        ok = 0;
-        set_status(status, PI_ERR_TIMEOUT);
-        break;
-      }
-    }
-    s_ok2 = ok;
-  }
-  __syncthreads();
-  return s_ok2 != 0;
 }
 
 // ------------------------------------------------------------------ TMA bulk copies

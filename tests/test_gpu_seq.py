@@ -87,7 +87,9 @@ def test_independent_steps_wrap_the_table(balance, monkeypatch):
     check_steps(layers, J, x, False, y, mask, cnt)
 
 
-def test_many_steps_one_launch():
+@pytest.mark.parametrize("balance", ["0", "1"])
+def test_many_steps_one_launch(balance, monkeypatch):
+    monkeypatch.setenv("PI_SEQ_BALANCE", balance)
     layers = tiny_layers(2, seed=23)
     J = 301
     x = synth.gen_x(23, 0, J, 1024)
@@ -105,6 +107,23 @@ def test_gated_bf16_llama_shape():
         check_steps([D], 3, x, False, y, mask, cnt)
         del D
         torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("balance", ["0", "1"])
+def test_opt67_shape_is_reproducible(balance, monkeypatch):
+    # every sum has a fixed order (with balancing too: the split of the cold
+    # work depends only on the lists), so two launches give the same bits;
+    # and the steps obey the oracle's rules
+    monkeypatch.setenv("PI_SEQ_BALANCE", balance)
+    L = synth.make_layer(4096, 16384, 128, "f16", alpha=0.9, density=0.06, seed=2)
+    D = DevLayer(L, DEV, hot_prefix=304, packed=True)
+    J = 6
+    x = synth.gen_x(26, 0, J, 4096)
+    y, mask, cnt = run_seq([D], J, x, chain=False)
+    y2, mask2, cnt2 = run_seq([D], J, x, chain=False)
+    assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
+    assert np.array_equal(mask, mask2) and np.array_equal(cnt, cnt2)
+    check_steps([D], J, x, False, y, mask, cnt)
 
 
 def test_opt67_shape_matches_layer_decode():
