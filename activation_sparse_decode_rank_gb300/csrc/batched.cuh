@@ -119,6 +119,7 @@ __device__ __forceinline__ void split16(float v, uint16_t* hi, uint16_t* lo) {
 template <int DT, int TB>
 __global__ void __launch_bounds__(256) bpu_partial_kernel(const uint16_t* Bm, const float* x, int d,
                                                           int r, int batch, int G, float* part) {
+  pdl_enter();
   extern __shared__ __align__(16) float xs[];  // [batch][w]
   const int c = blockIdx.x, tid = threadIdx.x, nch = d >> 3;
   const int q0 = (int)((long long)c * nch / G), q1 = (int)((long long)(c + 1) * nch / G);
@@ -158,6 +159,7 @@ __global__ void __launch_bounds__(256) bpu_partial_kernel(const uint16_t* Bm, co
 template <int DT>
 __global__ void __launch_bounds__(256) bpu_reduce_kernel(const float* part, int r, int batch, int bp,
                                                          int G, uint16_t* uhi, uint16_t* ulo) {
+  pdl_enter();
   __shared__ float ws[8][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * 32 + lane;  // t * r + k
@@ -189,6 +191,7 @@ template <int DT, int MT>
 __global__ void __launch_bounds__(256) blogit_kernel(const uint16_t* A, const float* b1,
                                                      const uint16_t* uhi, const uint16_t* ulo, int n,
                                                      int r, int batch, int bp, float* logits) {
+  pdl_enter();
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rowb = 2 * r + 16;
@@ -250,6 +253,7 @@ __global__ void __launch_bounds__(256) blogit_kernel(const uint16_t* A, const fl
 // xhi/xlo[t][j] = split(x[t][j]) for t < batch, 0 for padded rows.
 template <int DT>
 __global__ void bsplit_x_kernel(const BatchArgs a) {
+  pdl_enter();
   const long long tot = (long long)a.bp * a.d;
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < tot;
        e += (long long)gridDim.x * blockDim.x) {
@@ -276,6 +280,7 @@ __host__ __device__ constexpr int bup_stage_bytes(int bp) {
 
 template <int DT, bool GATED, int MT, int BK>
 __global__ void __launch_bounds__(512, 1) bup_kernel(const BatchArgs a) {
+  pdl_enter();
   constexpr int kRowB = bup_row_bytes<BK>();
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -434,6 +439,7 @@ __host__ __device__ inline int bdn_stage_bytes(int cw, int bp) {
 
 template <int DT, int MT>
 __global__ void __launch_bounds__(512, 1) bdown_kernel(const BatchArgs a) {
+  pdl_enter();
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x / a.slices, s = blockIdx.x - g * a.slices;
@@ -572,6 +578,7 @@ __global__ void __launch_bounds__(512, 1) bdown_kernel(const BatchArgs a) {
 
 // ---------------------------------------------------------------- phase 3
 __global__ void bsum_kernel(const BatchArgs a) {
+  pdl_enter();
   const long long tot = (long long)a.batch * a.d;
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < tot;
        e += (long long)gridDim.x * blockDim.x) {

@@ -138,6 +138,14 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+// First statement of a kernel in a launch chain: wait for the previous
+// kernel in the stream (its writes visible), then let the next kernel launch
+// (its blocks wait at their own first statement).  Without a programmatic
+// launch attribute both return at once.
+__device__ __forceinline__ void pdl_enter() {
+  pdl_wait();
+  pdl_trigger();
+}
 
 // Barrier among the kThreads compute threads only (the producer warp keeps
 // running its own loop).

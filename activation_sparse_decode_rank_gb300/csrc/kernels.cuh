@@ -879,6 +879,7 @@ __device__ __forceinline__ uint32_t token_mask(const float* logits, int n, int b
 
 __global__ void __launch_bounds__(kCB) cu_count_kernel(const float* logits, int n, int batch,
                                                        int want_union, int* scr, int nb) {
+  pdl_enter();
   __shared__ int wc[kCSeries][kCB / 32];
   const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t m = token_mask(logits, n, batch, b * kCB + tid);
@@ -897,6 +898,7 @@ __global__ void __launch_bounds__(kCB) cu_count_kernel(const float* logits, int 
 }
 
 __global__ void __launch_bounds__(1024) cu_scan_kernel(int* scr, int nb, int batch, int want_union) {
+  pdl_enter();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int s = warp; s < kCSeries; s += 32) {
     if (!(s < batch || (s == 32 && want_union))) continue;
@@ -922,6 +924,7 @@ __global__ void __launch_bounds__(kCB) cu_write_kernel(const float* logits, int 
                                                        const int* scr, int nb, int* idx, int* cnt,
                                                        int cap, int* uidx, int* ucnt,
                                                        uint32_t* tmask, int* status) {
+  pdl_enter();
   __shared__ int wc[kCSeries][kCB / 32];
   __shared__ unsigned wb[kCSeries][kCB / 32];
   const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;

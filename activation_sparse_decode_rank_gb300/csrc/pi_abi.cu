@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <mutex>
+#include <utility>
 #include <string>
 #include <unordered_map>
 
@@ -161,6 +162,26 @@ int launch_mode() {
     g_launch_mode = (e && std::string(e) == "cooperative") ? 0 : 1;
   }
   return g_launch_mode;
+}
+
+// Launch of one kernel of a chain with programmatic dependent launch: the
+// kernel may be scheduled while the previous kernel in the stream runs and
+// waits for it at its first statement (pdl_enter), so the chain pays no
+// launch gap between its kernels.  Returns the launch's CUDA error.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_chain(void (*k)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                         cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, std::forward<Args>(args)...);
 }
 
 pi_status ensure_smem(const void* fn, int bytes) {
@@ -371,9 +392,9 @@ pi_status launch_batched(const pi_ffn_desc& D, const pi_layer_weights& w, const 
   const bool bf = D.dtype == PI_BF16;
   const bool m2 = a.bp == 32;
   // phase 0: split x
-  if (bf) bsplit_x_kernel<1><<<di.sms * 4, 256, 0, st>>>(a);
-  else bsplit_x_kernel<0><<<di.sms * 4, 256, 0, st>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
+  if (launch_chain(bf ? bsplit_x_kernel<1> : bsplit_x_kernel<0>, di.sms * 4, 256, 0, st, a) !=
+      cudaSuccess)
+    return PI_ERR_CUDA;
   // phase 1
   const int nw = D.gated ? 2 : 1;
   // plain layers take 256-column chunks when d allows (fewer pipeline steps
@@ -415,8 +436,7 @@ pi_status launch_batched(const pi_ffn_desc& D, const pi_layer_weights& w, const 
   if (smem_launch + 1024 > di.smem_optin) return PI_ERR_SHAPE;
   s = ensure_smem(reinterpret_cast<const void*>(f1), smem_launch);
   if (s != PI_OK) return s;
-  f1<<<a.P, 512, smem_launch, st>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
+  if (launch_chain(f1, a.P, 512, smem_launch, st, a) != cudaSuccess) return PI_ERR_CUDA;
   // phase 2
   const int smem2 = kBStages * bdn_stage_bytes(a.cw, a.bp);
   Fn f2 = bf ? (m2 ? bdown_kernel<1, 2> : bdown_kernel<1, 1>)
@@ -424,11 +444,9 @@ pi_status launch_batched(const pi_ffn_desc& D, const pi_layer_weights& w, const 
   if (smem2 + 1024 > di.smem_optin || a.cw / 8 > 64) return PI_ERR_SHAPE;
   s = ensure_smem(reinterpret_cast<const void*>(f2), smem2);
   if (s != PI_OK) return s;
-  f2<<<kGroups2 * a.slices, 512, smem2, st>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
+  if (launch_chain(f2, kGroups2 * a.slices, 512, smem2, st, a) != cudaSuccess) return PI_ERR_CUDA;
   // phase 3
-  bsum_kernel<<<di.sms * 4, 256, 0, st>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
+  if (launch_chain(bsum_kernel, di.sms * 4, 256, 0, st, a) != cudaSuccess) return PI_ERR_CUDA;
   return PI_OK;
 }
 
@@ -583,19 +601,15 @@ pi_status pi_predict(const pi_ffn_desc* desc, const void* A, const void* Bm, con
     const bool bf = D.dtype == PI_BF16;
     const uint16_t* Bh = static_cast<const uint16_t*>(Bm);
     const bool tb8 = batch <= 8;
-    if (!bf) {
-      if (tb8) bpu_partial_kernel<0, 8><<<G, 256, smem1, st>>>(Bh, x, D.d, D.r, batch, G, part);
-      else bpu_partial_kernel<0, 32><<<G, 256, smem1, st>>>(Bh, x, D.d, D.r, batch, G, part);
-    } else {
-      if (tb8) bpu_partial_kernel<1, 8><<<G, 256, smem1, st>>>(Bh, x, D.d, D.r, batch, G, part);
-      else bpu_partial_kernel<1, 32><<<G, 256, smem1, st>>>(Bh, x, D.d, D.r, batch, G, part);
-    }
-    if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
+    auto fp = bf ? (tb8 ? bpu_partial_kernel<1, 8> : bpu_partial_kernel<1, 32>)
+                 : (tb8 ? bpu_partial_kernel<0, 8> : bpu_partial_kernel<0, 32>);
+    if (launch_chain(fp, G, 256, smem1, st, Bh, x, D.d, D.r, batch, G, part) != cudaSuccess)
+      return PI_ERR_CUDA;
     const int bp = L.bp;
     const unsigned gr = (unsigned)((bp * D.r + 31) / 32);
-    if (!bf) bpu_reduce_kernel<0><<<gr, 256, 0, st>>>(part, D.r, batch, bp, G, uhi, ulo);
-    else bpu_reduce_kernel<1><<<gr, 256, 0, st>>>(part, D.r, batch, bp, G, uhi, ulo);
-    if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
+    if (launch_chain(bf ? bpu_reduce_kernel<1> : bpu_reduce_kernel<0>, gr, 256, 0, st,
+                     (const float*)part, D.r, batch, bp, G, uhi, ulo) != cudaSuccess)
+      return PI_ERR_CUDA;
     const int smem2 = (kLT + 2 * bp) * (2 * D.r + 16);
     using LFn = void (*)(const uint16_t*, const float*, const uint16_t*, const uint16_t*, int, int,
                          int, int, float*);
@@ -603,9 +617,10 @@ pi_status pi_predict(const pi_ffn_desc* desc, const void* A, const void* Bm, con
                 : (bp == 32 ? blogit_kernel<0, 2> : blogit_kernel<0, 1>);
     s = ensure_smem(reinterpret_cast<const void*>(fl), smem2);
     if (s != PI_OK) return s;
-    fl<<<(unsigned)((D.n + kLT - 1) / kLT), 256, smem2, st>>>(
-        static_cast<const uint16_t*>(A), b1, uhi, ulo, D.n, D.r, batch, bp, logits);
-    if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
+    if (launch_chain(fl, (unsigned)((D.n + kLT - 1) / kLT), 256, smem2, st,
+                     static_cast<const uint16_t*>(A), b1, (const uint16_t*)uhi,
+                     (const uint16_t*)ulo, D.n, D.r, batch, bp, logits) != cudaSuccess)
+      return PI_ERR_CUDA;
     return PI_OK;
   }
   float* u = reinterpret_cast<float*>(static_cast<char*>(ws) + L.u);
@@ -655,11 +670,12 @@ pi_status pi_compact(const float* logits, int32_t n, int32_t batch, int32_t* idx
     int* scr = reinterpret_cast<int*>(static_cast<char*>(ws) + ((ws_bytes - need) & ~(size_t)15));
     const int nb = (n + kCB - 1) / kCB;
     const int wu = union_idx ? 1 : 0;
-    cu_count_kernel<<<nb, kCB, 0, st>>>(logits, n, batch, wu, scr, nb);
-    cu_scan_kernel<<<1, 1024, 0, st>>>(scr, nb, batch, wu);
-    cu_write_kernel<<<nb, kCB, 0, st>>>(logits, n, batch, scr, nb, idx, cnt, cap, union_idx,
-                                        union_cnt, tok_mask, dev_status);
-    if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
+    if (launch_chain(cu_count_kernel, nb, kCB, 0, st, logits, n, batch, wu, scr, nb) !=
+            cudaSuccess ||
+        launch_chain(cu_scan_kernel, 1, 1024, 0, st, scr, nb, batch, wu) != cudaSuccess ||
+        launch_chain(cu_write_kernel, nb, kCB, 0, st, logits, n, batch, (const int*)scr, nb, idx,
+                     cnt, cap, union_idx, union_cnt, tok_mask, dev_status) != cudaSuccess)
+      return PI_ERR_CUDA;
     return PI_OK;
   }
   // without a workspace: one block per token, one block for the union

@@ -64,6 +64,7 @@ __device__ __forceinline__ void tc_ld4(uint32_t (&r)[4], uint32_t taddr) {
 
 template <int DT, bool GATED, int MH>
 __global__ void __launch_bounds__(512, 1) bup_tc_kernel(const BatchArgs a) {
+  pdl_enter();
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ uint32_t s_taddr;
   __shared__ __align__(8) uint64_t s_mbar[kTcStages];
