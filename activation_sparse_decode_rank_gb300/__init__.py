@@ -68,6 +68,23 @@ class pi_layer_weights(ctypes.Structure):
                 ("W1", ctypes.c_void_p), ("W2", ctypes.c_void_p), ("b2", ctypes.c_void_p)]
 
 
+PI_PATH_FUSED, PI_PATH_PER_TOKEN, PI_PATH_UNION, PI_PATH_DENSE = range(4)
+PI_PATHS, PI_COST_TIERS = 4, 4
+PATH_NAMES = ("fused", "per_token", "union", "dense")
+
+
+class pi_cost_model(ctypes.Structure):
+    _fields_ = [("tier_max_batch", ctypes.c_int32 * PI_COST_TIERS),
+                ("fixed_us", (ctypes.c_double * PI_COST_TIERS) * PI_PATHS),
+                ("gbs", (ctypes.c_double * PI_COST_TIERS) * PI_PATHS)]
+
+
+class pi_plan(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int32), ("est_us", ctypes.c_double * PI_PATHS),
+                ("bytes", ctypes.c_double * PI_PATHS), ("active_rows", ctypes.c_double),
+                ("union_rows", ctypes.c_double)]
+
+
 # Names and argument lists of the C entry points (include/pi.h).
 _P, _I32, _SZ, _I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_int64
 _DESC = ctypes.POINTER(pi_ffn_desc)
@@ -89,6 +106,10 @@ SIGNATURES = {
     "pi_profile_counts": (ctypes.c_int, [_P, _I32, _I32, _P, _P]),
     "pi_hot_order": (ctypes.c_int, [_P, _I32, _P, _P]),
     "pi_permute_neurons": (ctypes.c_int, [_DESC, _W, _P, _W, _P, _P]),
+    "pi_default_cost_model": (None, [ctypes.POINTER(pi_cost_model)]),
+    "pi_plan_dispatch": (ctypes.c_int, [_DESC, _I32, ctypes.POINTER(ctypes.c_float),
+                                        ctypes.c_float, _I32, ctypes.POINTER(pi_cost_model),
+                                        ctypes.POINTER(pi_plan)]),
 }
 
 
@@ -223,6 +244,23 @@ def pi_hot_order(counts, n, perm, stream=None) -> int:
 def pi_permute_neurons(desc, src, perm, dst, dev_status, stream=None) -> int:
     return lib().pi_permute_neurons(ctypes.byref(desc), ctypes.byref(src), _ptr(perm),
                                     ctypes.byref(dst), _ptr(dev_status), _stream(stream))
+
+
+def pi_default_cost_model(out: pi_cost_model) -> None:
+    lib().pi_default_cost_model(ctypes.byref(out))
+
+
+def pi_plan_dispatch(desc, batch, p_active, density, allow_dense, model, out) -> int:
+    """p_active: None or a host float32 numpy array of n values; model: None
+    (the built-in one) or a pi_cost_model; out: a pi_plan filled in place."""
+    pa = None
+    if p_active is not None:
+        import numpy as np
+        arr = np.ascontiguousarray(p_active, dtype=np.float32)
+        pa = arr.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
+    return lib().pi_plan_dispatch(ctypes.byref(desc), int(batch), pa, float(density),
+                                  int(allow_dense), ctypes.byref(model) if model is not None
+                                  else None, ctypes.byref(out))
 
 
 def pi_pack_weights(desc, W1, W2, packed, stream=None) -> int:

@@ -12,6 +12,7 @@
 #include "kernels.cuh"
 #include "batched.cuh"
 #include "seq.cuh"
+#include "plan.cuh"
 #include "tc.cuh"
 
 using namespace pik;
@@ -551,6 +552,82 @@ size_t pi_workspace_size(const pi_ffn_desc* desc, int32_t batch) {
   if (check_desc(desc) != PI_OK) return 0;
   if (batch < 1 || batch > kMaxBatch) return 0;
   return ws_layout(*desc, batch).total;
+}
+
+void pi_default_cost_model(pi_cost_model* out) {
+  if (!out) return;
+  *out = pi_cost_model{};
+  const int32_t tiers[PI_COST_TIERS] = {1, 4, 16, 32};
+  // per tier (batch <= 1, 4, 16, 32): fixed microseconds and GB/s of a
+  // least-squares fit to the measured sweep (five densities per batch)
+  const double fused_fix = 15.4, fused_gbs = 4610.0;
+  const double union_fix[PI_COST_TIERS] = {41.3, 41.3, 43.9, 51.6};
+  const double union_gbs[PI_COST_TIERS] = {2628.0, 2628.0, 2405.0, 1826.0};
+  const double dense_gbs[PI_COST_TIERS] = {5926.0, 2882.0, 2846.0, 2110.0};
+  for (int t = 0; t < PI_COST_TIERS; ++t) {
+    out->tier_max_batch[t] = tiers[t];
+    out->fixed_us[PI_PATH_FUSED][t] = out->fixed_us[PI_PATH_PER_TOKEN][t] = fused_fix;
+    out->gbs[PI_PATH_FUSED][t] = out->gbs[PI_PATH_PER_TOKEN][t] = fused_gbs;
+    out->fixed_us[PI_PATH_UNION][t] = union_fix[t];
+    out->gbs[PI_PATH_UNION][t] = union_gbs[t];
+    out->fixed_us[PI_PATH_DENSE][t] = 3.0;
+    out->gbs[PI_PATH_DENSE][t] = dense_gbs[t];
+  }
+}
+
+pi_status pi_plan_dispatch(const pi_ffn_desc* desc, int32_t batch, const float* p_active,
+                           float density, int32_t allow_dense, const pi_cost_model* model,
+                           pi_plan* out) {
+  if (!desc || !out) return PI_ERR_NULL;
+  pi_status s = check_desc(desc);
+  if (s != PI_OK) return s;
+  if (batch < 1 || batch > 32) return PI_ERR_SHAPE;
+  if (!p_active && !(density >= 0.f && density <= 1.f)) return PI_ERR_SHAPE;
+  pi_cost_model M;
+  if (model) M = *model;
+  else pi_default_cost_model(&M);
+  for (int t = 0; t < PI_COST_TIERS; ++t) {
+    if (t > 0 && M.tier_max_batch[t] < M.tier_max_batch[t - 1]) return PI_ERR_SHAPE;
+    for (int k = 0; k < PI_PATHS; ++k)
+      if (!(M.gbs[k][t] > 0.0)) return PI_ERR_SHAPE;
+  }
+  const pi_ffn_desc& D = *desc;
+  double active = 0.0, uni = 0.0;
+  plan_expected_rows(p_active, D.n, density, batch, &active, &uni);
+  const double e = 2.0, m = D.gated ? 3.0 : 2.0;
+  const double pred = (double)D.n * D.r * e + (double)D.r * D.d * e + 4.0 * D.n;
+  const double row = m * D.d * e;
+  const int t = plan_tier(M, batch);
+  pi_plan P{};
+  for (int k = 0; k < PI_PATHS; ++k) P.est_us[k] = P.bytes[k] = -1.0;
+  P.active_rows = active;
+  P.union_rows = uni;
+  if (batch == 1) {
+    P.bytes[PI_PATH_FUSED] = pred + active * row;
+    P.est_us[PI_PATH_FUSED] = plan_time_us(M.fixed_us[PI_PATH_FUSED][0], P.bytes[PI_PATH_FUSED],
+                                           M.gbs[PI_PATH_FUSED][0]);
+  } else {
+    const double one = pred + active * row;
+    P.bytes[PI_PATH_PER_TOKEN] = batch * one;
+    P.est_us[PI_PATH_PER_TOKEN] =
+        batch * plan_time_us(M.fixed_us[PI_PATH_PER_TOKEN][0], one, M.gbs[PI_PATH_PER_TOKEN][0]);
+    if (D.d % 128 == 0) {
+      P.bytes[PI_PATH_UNION] = pred + uni * row;
+      P.est_us[PI_PATH_UNION] = plan_time_us(M.fixed_us[PI_PATH_UNION][t], P.bytes[PI_PATH_UNION],
+                                             M.gbs[PI_PATH_UNION][t]);
+    }
+  }
+  if (allow_dense) {
+    P.bytes[PI_PATH_DENSE] = (double)D.n * row;
+    P.est_us[PI_PATH_DENSE] = plan_time_us(M.fixed_us[PI_PATH_DENSE][t], P.bytes[PI_PATH_DENSE],
+                                           M.gbs[PI_PATH_DENSE][t]);
+  }
+  int best = -1;
+  for (int k = 0; k < PI_PATHS; ++k)  // ties go to the lower path number
+    if (P.est_us[k] >= 0.0 && (best < 0 || P.est_us[k] < P.est_us[best])) best = k;
+  P.path = static_cast<pi_path>(best);
+  *out = P;
+  return PI_OK;
 }
 
 const char* pi_status_string(pi_status s) {

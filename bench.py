@@ -718,6 +718,7 @@ def run_sweep(args):
                 "sparse_gbs": alg / res["sparse"] / 1e3, "sparse_frac": alg / res["sparse"] / 1e3 / peak,
                 "dense_gbs": dense_alg / res["dense"] / 1e3,
                 "dense_frac": dense_alg / res["dense"] / 1e3 / peak,
+                "plan": sweep_plan(pi, desc, B, pz, res),
             })
             del xs, ws
         del reps, wts, base
@@ -735,6 +736,7 @@ def run_sweep(args):
         if c is None and pts and pts[-1]["speedup_vs_dense"] >= 1.0:
             c = f"> {pts[-1]['density']}"
         cross[str(B)] = c
+    agree = [p["plan"]["agrees"] for p in points]
     peak, peak_kind = measured_peaks()
     print(json.dumps({
         "metric": "batched sparse-FFN decode: us per step and tokens/s vs the dense FFN",
@@ -742,9 +744,28 @@ def run_sweep(args):
         "config": {"d": d, "n": n, "r": r, "weights": w["dtype"], "layout": "packed",
                    "l2": "2 alternating weight replicas of 0.43 GB each"},
         "peak_gbs": peak, "peak_kind": peak_kind, "points": points,
-        "crossover_density_per_batch": cross, "clocks": clocks, "csrc_hash": csrc_hash(),
+        "crossover_density_per_batch": cross,
+        "plan_agreement": {"points": len(agree), "agree": int(sum(agree)),
+                           "how": "pi_plan_dispatch (built-in cost model, the generator's p_i, "
+                                  "dense allowed) picks dense or the sparse path; agrees when "
+                                  "the measured faster of the two is the same"},
+        "clocks": clocks, "csrc_hash": csrc_hash(),
     }), flush=True)
     return 0
+
+
+def sweep_plan(pi, desc, B, pz, res):
+    """The dispatch plan of one sweep point against its measurement."""
+    out = pi.pi_plan()
+    pi.check(pi.pi_plan_dispatch(desc, B, pz.astype(np.float32), 0.0, 1, None, out),
+             "pi_plan_dispatch")
+    sp = pi.PI_PATH_FUSED if B == 1 else pi.PI_PATH_UNION
+    plan_dense = out.est_us[pi.PI_PATH_DENSE] < out.est_us[sp]
+    meas_dense = res["dense"] < res["sparse"]
+    return {"path": pi.PATH_NAMES[out.path], "sparse_est_us": out.est_us[sp],
+            "dense_est_us": out.est_us[pi.PI_PATH_DENSE],
+            "per_token_est_us": out.est_us[pi.PI_PATH_PER_TOKEN],
+            "union_rows_est": out.union_rows, "agrees": plan_dense == meas_dense}
 
 
 def run_reorder(args):

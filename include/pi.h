@@ -291,6 +291,72 @@ pi_status pi_permute_neurons(const pi_ffn_desc* desc, const pi_layer_weights* sr
 pi_status pi_pack_weights(const pi_ffn_desc* desc, const void* W1, const void* W2,
                           void* packed, pi_stream stream);
 
+/* ---------------------------------------------------------------- dispatch plan
+ * Density / batch-aware choice of the decode path ("Efficient,
+ * VRAM-Constrained xLM Inference on Clients", section "Methodology, A.
+ * Pipelined Sharding": per tier of tokens per step, a time estimator built
+ * on bytes moved and measured rates picks the cheapest plan).  Host only: no
+ * GPU work, no allocation.
+ *
+ * Paths:
+ *   PI_PATH_FUSED     batch 1: pi_layer_decode (one persistent launch);
+ *   PI_PATH_PER_TOKEN batch > 1 as `batch` batch-1 fused decodes;
+ *   PI_PATH_UNION     batch 2..32: pi_layer_decode's union of the tokens'
+ *                     active rows on the tensor cores (needs d % 128 == 0);
+ *   PI_PATH_DENSE     pi_dense_ffn: every row, no predictor.  It computes the
+ *                     plain dense FFN, not the predicted-sparse result, so a
+ *                     plan offers it only when allow_dense != 0.
+ * The first three give the same result (each token's own predicted set).
+ *
+ * Expected rows: with p_i = P(neuron i active for a token) -- p_active[i]
+ * (host array of n values, e.g. pi_profile_counts / profiled tokens), or
+ * `density` for every neuron when p_active is NULL -- a token's active rows
+ * are sum_i p_i and a batch's union sum_i (1 - (1 - p_i)^batch) (tokens
+ * independent).  Bytes per step: predictor P = n r e + r d e + 4 n, a row
+ * R = m d e (e = 2, m = 2 plain / 3 gated): FUSED P + active R; PER_TOKEN
+ * batch x (P + active R); UNION P + union R; DENSE n R.
+ * Time = fixed_us + bytes / (gbs x 1e3) in microseconds, with the path's
+ * constants of the batch's tier (PER_TOKEN: batch x FUSED's tier-0 time). */
+typedef enum {
+  PI_PATH_FUSED = 0,
+  PI_PATH_PER_TOKEN = 1,
+  PI_PATH_UNION = 2,
+  PI_PATH_DENSE = 3
+} pi_path;
+
+#define PI_PATHS 4
+#define PI_COST_TIERS 4
+
+/* Measured cost of each path per batch tier.  tier_max_batch ascending: a
+ * batch uses the first tier whose max is >= batch (the last tier above). */
+typedef struct {
+  int32_t tier_max_batch[PI_COST_TIERS];
+  double fixed_us[PI_PATHS][PI_COST_TIERS];
+  double gbs[PI_PATHS][PI_COST_TIERS];  /* GB/s, > 0 */
+} pi_cost_model;
+
+typedef struct {
+  pi_path path;                /* the available path of least estimated time */
+  double est_us[PI_PATHS];     /* estimate per path; -1 when not available */
+  double bytes[PI_PATHS];      /* weight bytes per step behind each estimate; -1 n/a */
+  double active_rows;          /* expected active neurons per token */
+  double union_rows;           /* expected union of the batch's active neurons */
+} pi_plan;
+
+/* The built-in model: fitted on one GB300 (measured copy peak 6.78 TB/s) to
+ * the density x batch sweep of the OPT-13B-shaped layer (d 5120, n 20480,
+ * r 192, fp16; within 5.3 % of every measured point).  Other shapes move
+ * the fixed costs (grid-wide waits, launches) by some microseconds. */
+void pi_default_cost_model(pi_cost_model* out);
+
+/* Fills *out for one layer shape and batch (1..32).  model NULL: the
+ * built-in one.  Errors: PI_ERR_NULL (desc or out), PI_ERR_SHAPE (bad desc,
+ * batch outside 1..32, density outside [0, 1] without p_active, a model
+ * rate <= 0 or tiers not ascending). */
+pi_status pi_plan_dispatch(const pi_ffn_desc* desc, int32_t batch, const float* p_active,
+                           float density, int32_t allow_dense, const pi_cost_model* model,
+                           pi_plan* out);
+
 /* Static text of a status code. */
 const char* pi_status_string(pi_status s);
 

@@ -1,0 +1,140 @@
+"""Density / batch-aware dispatch plan (pi_plan_dispatch): host logic, no GPU.
+
+The expected rows are pinned by exact enumeration over every activation
+outcome of a tiny layer; the rest checks the byte counts, the availability
+of each path, the choice of the cheapest estimate and the error channel.
+"""
+import itertools
+
+import numpy as np
+import pytest
+
+import activation_sparse_decode_rank_gb300 as pi
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    pi.build()
+    pi.lib()
+
+
+def plan(desc, batch, p=None, density=0.0, allow_dense=1, model=None):
+    out = pi.pi_plan()
+    st = pi.pi_plan_dispatch(desc, batch, p, density, allow_dense, model, out)
+    return st, out
+
+
+def test_expected_rows_match_exact_enumeration():
+    # every outcome of n neurons x B tokens, each neuron active with its own
+    # probability, independently: the mean of |union| and of a token's count
+    p = np.array([0.25, 0.5, 0.125, 0.75], dtype=np.float32)
+    n, B = p.size, 3
+    desc = pi.make_desc(128, n, 8)
+    eu = ea = 0.0
+    for bits in itertools.product((0, 1), repeat=n * B):
+        m = np.array(bits).reshape(B, n)
+        pr = np.prod(np.where(m == 1, p, 1 - p).astype(np.float64))
+        eu += pr * m.any(axis=0).sum()
+        ea += pr * m[0].sum()
+    st, out = plan(desc, B, p)
+    assert st == pi.PI_OK
+    assert out.union_rows == pytest.approx(eu, rel=1e-12)
+    assert out.active_rows == pytest.approx(ea, rel=1e-12)
+
+
+def test_uniform_density_equals_a_flat_profile():
+    desc = pi.make_desc(5120, 20480, 192)
+    for B in (1, 2, 7, 32):
+        for rho in (0.0, 0.02, 0.3, 1.0):
+            _, a = plan(desc, B, None, rho)
+            _, b = plan(desc, B, np.full(20480, rho, np.float32))
+            assert a.union_rows == pytest.approx(b.union_rows, rel=1e-9, abs=1e-6)
+            assert a.active_rows == pytest.approx(b.active_rows, rel=1e-9, abs=1e-6)
+    _, z = plan(desc, 4, None, 0.0)
+    assert z.union_rows == 0.0 and z.active_rows == 0.0
+    _, f = plan(desc, 4, None, 1.0)
+    assert f.union_rows == 20480 and f.active_rows == 20480
+
+
+def test_union_grows_with_batch_and_stays_bounded():
+    rng = np.random.default_rng(0)
+    p = (rng.random(4096) ** 4).astype(np.float32)
+    desc = pi.make_desc(1024, 4096, 64)
+    prev = 0.0
+    for B in range(1, 33):
+        _, o = plan(desc, B, p)
+        assert o.union_rows >= prev - 1e-9
+        assert o.union_rows <= min(4096.0, B * o.active_rows) + 1e-6
+        assert o.union_rows >= o.active_rows - 1e-6
+        prev = o.union_rows
+
+
+def test_bytes_and_availability():
+    d, n, r = 5120, 20480, 192
+    desc = pi.make_desc(d, n, r)
+    pred = n * r * 2 + r * d * 2 + 4 * n
+    row = 2 * d * 2
+    _, o1 = plan(desc, 1, None, 0.1, allow_dense=0)
+    assert o1.path == pi.PI_PATH_FUSED
+    assert list(o1.est_us)[1:] == [-1.0, -1.0, -1.0]
+    assert o1.bytes[pi.PI_PATH_FUSED] == pytest.approx(pred + 0.1 * n * row)
+    _, o4 = plan(desc, 4, None, 0.1, allow_dense=1)
+    assert o4.est_us[pi.PI_PATH_FUSED] == -1.0
+    assert o4.bytes[pi.PI_PATH_PER_TOKEN] == pytest.approx(4 * (pred + 0.1 * n * row))
+    assert o4.bytes[pi.PI_PATH_UNION] == pytest.approx(pred + o4.union_rows * row)
+    assert o4.bytes[pi.PI_PATH_DENSE] == pytest.approx(n * row)
+    gated = pi.make_desc(d, n, r, gated=True)
+    _, og = plan(gated, 4, None, 0.1)
+    assert og.bytes[pi.PI_PATH_DENSE] == pytest.approx(n * 3 * d * 2)
+    odd = pi.make_desc(1000, n, r)  # d % 128 != 0: no union path
+    _, oo = plan(odd, 4, None, 0.1)
+    assert oo.est_us[pi.PI_PATH_UNION] == -1.0 and oo.path != pi.PI_PATH_UNION
+
+
+def test_choice_is_the_least_estimate():
+    desc = pi.make_desc(5120, 20480, 192)
+    for B in (1, 2, 4, 9, 16, 32):
+        for rho in (0.01, 0.05, 0.2, 0.6):
+            for allow in (0, 1):
+                _, o = plan(desc, B, None, rho, allow)
+                ok = [(o.est_us[k], k) for k in range(pi.PI_PATHS) if o.est_us[k] >= 0]
+                assert o.path == min(ok)[1]
+                if not allow:
+                    assert o.est_us[pi.PI_PATH_DENSE] == -1.0
+
+
+def test_estimates_follow_the_model():
+    desc = pi.make_desc(4096, 16384, 128)
+    m = pi.pi_cost_model()
+    pi.pi_default_cost_model(m)
+    for t in range(pi.PI_COST_TIERS):
+        for k in range(pi.PI_PATHS):
+            m.fixed_us[k][t] = 10.0 * (k + 1)
+            m.gbs[k][t] = 1000.0 * (t + 1)
+    _, o = plan(desc, 5, None, 0.05, 1, m)  # batch 5: tier of batch <= 16 (index 2)
+    for k in (pi.PI_PATH_UNION, pi.PI_PATH_DENSE):
+        assert o.est_us[k] == pytest.approx(10.0 * (k + 1) + o.bytes[k] / (3000.0 * 1e3))
+    # per token: batch x the fused tier-0 estimate of one token
+    one = o.bytes[pi.PI_PATH_PER_TOKEN] / 5
+    assert o.est_us[pi.PI_PATH_PER_TOKEN] == pytest.approx(5 * (20.0 + one / 1e6))
+
+
+def test_errors():
+    desc = pi.make_desc(4096, 16384, 128)
+    out = pi.pi_plan()
+    assert pi.pi_plan_dispatch(desc, 0, None, 0.1, 1, None, out) == pi.PI_ERR_SHAPE
+    assert pi.pi_plan_dispatch(desc, 33, None, 0.1, 1, None, out) == pi.PI_ERR_SHAPE
+    assert pi.pi_plan_dispatch(desc, 4, None, 1.5, 1, None, out) == pi.PI_ERR_SHAPE
+    assert pi.pi_plan_dispatch(desc, 4, None, float("nan"), 1, None, out) == pi.PI_ERR_SHAPE
+    bad = pi.make_desc(4096, 16384, 7)
+    assert pi.pi_plan_dispatch(bad, 4, None, 0.1, 1, None, out) == pi.PI_ERR_SHAPE
+    m = pi.pi_cost_model()
+    pi.pi_default_cost_model(m)
+    m.gbs[pi.PI_PATH_UNION][1] = 0.0
+    assert pi.pi_plan_dispatch(desc, 4, None, 0.1, 1, m, out) == pi.PI_ERR_SHAPE
+    pi.pi_default_cost_model(m)
+    m.tier_max_batch[2] = 2
+    assert pi.pi_plan_dispatch(desc, 4, None, 0.1, 1, m, out) == pi.PI_ERR_SHAPE
+    L = pi.lib()
+    assert L.pi_plan_dispatch(None, 4, None, 0.1, 1, None, out) == pi.PI_ERR_NULL
+    assert L.pi_plan_dispatch(desc, 4, None, 0.1, 1, None, None) == pi.PI_ERR_NULL
