@@ -899,14 +899,15 @@ pi_status pi_decode_layers(const pi_ffn_desc* descs, const pi_layer_weights* lay
   if (!descs || !layers) return PI_ERR_NULL;
   if (R < 1 || R > kSeqMaxLayers || J < 1 || (chain != 0 && chain != 1)) return PI_ERR_SHAPE;
   pi_ffn_desc D = descs[0];
-  int hot_max = 0;
+  int hot_max = 0, r_max = 0;
   for (int l = 0; l < R; ++l) {
     const pi_ffn_desc& E = descs[l];
     pi_status s = check_desc(&E);
     if (s != PI_OK) return s;
-    if (E.d != D.d || E.n != D.n || E.r != D.r || E.dtype != D.dtype || E.gated != D.gated ||
+    if (E.d != D.d || E.n != D.n || E.dtype != D.dtype || E.gated != D.gated ||
         E.layout != D.layout)
       return PI_ERR_SHAPE;
+    if (E.r > r_max) r_max = E.r;
     s = check_weights(E, &layers[l], true);
     if (s != PI_OK) return s;
     if (E.hot_prefix > hot_max) hot_max = E.hot_prefix;
@@ -915,6 +916,7 @@ pi_status pi_decode_layers(const pi_ffn_desc* descs, const pi_layer_weights* lay
   const void* ps[] = {x, y, cnt_out, dev_status, ws};
   for (const void* p : ps)
     if (p && !aligned16(p)) return PI_ERR_ALIGN;
+  D.r = r_max;  // buffers and shared memory for the largest rank; each job uses its own
   const WsLayout L = ws_layout(D, 1);
   if (ws_bytes < L.total) return PI_ERR_WORKSPACE;
   DevInfo di;
@@ -964,6 +966,7 @@ pi_status pi_decode_layers(const pi_ffn_desc* descs, const pi_layer_weights* lay
     e.W2 = static_cast<const uint16_t*>(w.W2);  // NULL when packed (records hold both)
     e.b2 = w.b2;
     e.hot = descs[l].hot_prefix;
+    e.r = descs[l].r;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)P);

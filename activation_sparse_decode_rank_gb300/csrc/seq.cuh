@@ -50,7 +50,7 @@ struct SeqLayer {
   const uint16_t* W2;
   const float* b2;
   int hot;
-  int pad_;
+  int r;  // this layer's predictor rank (<= the launch's f.r, which sizes the buffers)
 };
 
 struct SeqArgs {
@@ -96,7 +96,6 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
 
   unsigned char* bms = slots + (size_t)(f.ns - 1) * f.slot_bytes;  // staged Bm columns
   FfnArgs a = f;  // the current job's weights
-  const int rc = f.r >> 3;
   int nh_c = 0;   // own hot neurons whose rows went to slots for the current job
 
   // The weights of job j that do not depend on its x.  prep_set points the
@@ -117,6 +116,7 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
     a.W2 = Lw.W2;
     a.b2 = Lw.b2;
     a.hot = Lw.hot;
+    a.r = Lw.r;
     nh_c = min(f.nh, (c < a.hot) ? (a.hot - 1 - c) / P + 1 : 0);
   };
   auto prep_issue = [&](int t0, int nt) {
@@ -137,21 +137,22 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
     if (t >= 0 && t < nt) {
       const int hot_own = (c < a.hot) ? (a.hot - 1 - c) / P + 1 : 0;
       if (sa.bm_smem)
-        for (int e = t; e < f.r * nq; e += nt) {
+        for (int e = t; e < a.r * nq; e += nt) {
           const int k = e / nq, q = e - k * nq;
           cp_async16(bms + (size_t)e * 16, a.Bm + (size_t)k * f.d + 8 * (q0 + q));
         }
       cp_async_commit();
       for (int k = nh_c + t; k < hot_own; k += nt) prefetch_neuron<GATED>(a, c + k * P);
       if (f.a_in_smem) {
+        const int rc = a.r >> 3;
         for (int e = t; e < rows * rc; e += nt) {
           const int jj = e / rc, q = e - jj * rc;
           cp_async16(As + (size_t)jj * f.a_stride + 16 * q,
-                     a.A + ((size_t)c + (size_t)jj * P) * f.r + 8 * q);
+                     a.A + ((size_t)c + (size_t)jj * P) * a.r + 8 * q);
         }
       } else {
         for (int jj = t; jj < rows; jj += nt)
-          prefetch_l2(a.A + ((size_t)c + (size_t)jj * P) * f.r, (size_t)f.r * 2);
+          prefetch_l2(a.A + ((size_t)c + (size_t)jj * P) * a.r, (size_t)a.r * 2);
       }
       for (int jj = t; jj < rows; jj += nt) cp_async4(b1s + jj, a.b1 + c + (size_t)jj * P);
       cp_async_commit();
@@ -179,7 +180,7 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
     cp_async_wait_group<1>();  // this job's staged Bm columns
     __syncthreads();
     // U: partial predictor stage 1 over the own columns, u_c[k] for k < r
-    if (tid < f.r) {
+    if (tid < a.r) {
       const uint16_t* row = a.Bm + (size_t)tid * f.d + 8 * q0;
       float acc = 0.f;
       for (int qb = 0; qb < nq; qb += 4) {  // batches of 4 pieces, loads first
@@ -221,9 +222,12 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
       reinterpret_cast<float4*>(xs)[i] = __ldcg(reinterpret_cast<const float4*>(xj) + i);
     if (tid < f.r) {
       // u[k] from its accumulator; block 0 clears the other buffer (last
-      // read by the previous job, before this job's first wait) for the next
-      const unsigned long long v = __ldcg(sa.uacc + ((size_t)(j & 1) * f.r + tid) * 16);
-      us[tid] = (float)((double)(long long)v * 2.3283064365386963e-10);  // x 2^-32
+      // read by the previous job, before this job's first wait) for the
+      // next, over the largest rank of the launch
+      if (tid < a.r) {
+        const unsigned long long v = __ldcg(sa.uacc + ((size_t)(j & 1) * f.r + tid) * 16);
+        us[tid] = (float)((double)(long long)v * 2.3283064365386963e-10);  // x 2^-32
+      }
       if (c == 0) sa.uacc[((size_t)((j + 1) & 1) * f.r + tid) * 16] = 0ull;
     }
     cp_async_wait_all();  // this job's staged predictor rows and biases

@@ -212,14 +212,18 @@ pi_status pi_layer_decode(const pi_ffn_desc* desc, const pi_layer_weights* w,
  * previous step finishes; a step's input is read only after the previous
  * step is complete.
  *   descs / layers: host arrays of R (1 <= R <= 128) layers with one shape
- *     (d, n, r, dtype, gated, layout equal; hot_prefix may differ);
- *     step j uses layer j % R.
+ *     (d, n, dtype, gated, layout equal); hot_prefix and the predictor rank
+ *     r may differ per layer (each layer's predictor sized by that layer's
+ *     skewness and sparsity: "PowerInfer: Quick Massive Language Mannequin
+ *     Serving with a Client-grade GPU", section "Adaptive Sparsity
+ *     Predictors"); step j uses layer j % R.
  *   chain = 1: a residual stack, x_0 = x [d], x_{j+1} = x_j + FFN_j(x_j),
  *     y[j] = x_{j+1};  chain = 0: independent steps, x [J][d] (one input
  *     per step), y[j] = FFN_j(x[j]).  y: [J][d] fp32.
  *   cnt_out: NULL or [J], active neurons of each step; mask_out: NULL or
  *     [J][n] bytes, 1 where the neuron was predicted active.
- *   ws: pi_workspace_size(&descs[0], 1) bytes.  Needs d / 8 <= 8 x the
+ *   ws: pi_workspace_size(desc, 1) bytes for a desc of the table with the
+ *   largest r (the size grows with r).  Needs d / 8 <= 8 x the
  *   number of SMs.  Device-side errors go to *dev_status as in
  *   pi_layer_decode.  The paper has no counterpart: it decodes one layer
  *   call at a time. */

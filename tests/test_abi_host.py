@@ -129,9 +129,13 @@ def test_decode_layers_host_validation(lib):
     assert f([d] * 129, [w] * 129, 1, P, 1, P, None, None, P, P, wsb) == pi.PI_ERR_SHAPE
     assert f([d], [w], 0, P, 1, P, None, None, P, P, wsb) == pi.PI_ERR_SHAPE
     assert f([d], [w], 4, P, 2, P, None, None, P, P, wsb) == pi.PI_ERR_SHAPE
-    # layers of different shapes; hot prefixes may differ
+    # layers of different shapes; hot prefixes and predictor ranks may differ,
+    # with a workspace sized for the largest rank
     e = pi.make_desc(1024, 4096, 128, "f16")
-    assert f([d, e], [w, w], 2, P, 1, P, None, None, P, P, wsb) == pi.PI_ERR_SHAPE
+    assert f([d, e], [w, w], 2, P, 1, P, None, None, P, P, wsb) == pi.PI_ERR_WORKSPACE
+    assert pi.pi_workspace_size(e, 1) > wsb
+    dd = pi.make_desc(2048, 4096, 64, "f16")
+    assert f([d, dd], [w, w], 2, P, 1, P, None, None, P, P, wsb) == pi.PI_ERR_SHAPE
     g = pi.make_desc(1024, 4096, 64, "f16", gated=True)
     assert f([d, g], [w, w], 2, P, 1, P, None, None, P, P, wsb) == pi.PI_ERR_SHAPE
     # predictor weights required; NULL / misaligned buffers; small workspace

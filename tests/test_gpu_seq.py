@@ -77,6 +77,31 @@ def test_stack_chain_tiny(packed, balance, monkeypatch):
     assert check_steps(layers, 4, x, True, y, mask, cnt) <= 8
 
 
+@pytest.mark.parametrize("chain", [True, False])
+def test_rank_per_layer(chain):
+    # each layer its own predictor rank (64, 16, 48, 32): the launch sizes
+    # its buffers for the largest, every step uses its layer's own
+    ranks = (64, 16, 48, 32)
+    layers = []
+    for l, r in enumerate(ranks):
+        L = synth.make_layer(1024, 4096, r, "f16", alpha=0.8, density=0.08, seed=27, layer=l)
+        layers.append(DevLayer(L, DEV, hot_prefix=90, packed=True))
+    J = 6
+    x = synth.gen_x(27, 0, 1 if chain else J, 1024)
+    d, n = 1024, 4096
+    y = torch.full((J, d), float("nan"), device=DEV)
+    cnt = torch.full((max(J, 4),), -1, dtype=torch.int32, device=DEV)
+    mask = torch.full((J, n), 7, dtype=torch.uint8, device=DEV)
+    st = zeros_i32(1, DEV)
+    big = max(layers, key=lambda D: D.desc.r).desc
+    ws = pi.workspace(big, 1, DEV)
+    pi.check(pi.pi_decode_layers([D.desc for D in layers], [D.w for D in layers], J, up(x, DEV),
+                                 int(chain), y, cnt, mask, st, ws), "pi_decode_layers")
+    torch.cuda.synchronize()
+    assert int(st[0]) == 0, pi.status_string(int(st[0]))
+    check_steps(layers, J, x, chain, y.cpu().numpy(), mask.cpu().numpy(), cnt.cpu().numpy()[:J])
+
+
 @pytest.mark.parametrize("balance", ["0", "1"])
 def test_independent_steps_wrap_the_table(balance, monkeypatch):
     monkeypatch.setenv("PI_SEQ_BALANCE", balance)
