@@ -920,17 +920,40 @@ __global__ void __launch_bounds__(1024) cu_scan_kernel(int* scr, int nb, int bat
   }
 }
 
+// fused = 1: scr holds the raw per-block counts of cu_count_kernel (no
+// cu_scan_kernel ran); every block sums the counts of the blocks before it
+// itself (integer sums: any order gives the same offsets).  Meant for few
+// blocks (the work is quadratic in nb).
 __global__ void __launch_bounds__(kCB) cu_write_kernel(const float* logits, int n, int batch,
                                                        const int* scr, int nb, int* idx, int* cnt,
                                                        int cap, int* uidx, int* ucnt,
-                                                       uint32_t* tmask, int* status) {
+                                                       uint32_t* tmask, int* status, int fused) {
   pdl_enter();
   __shared__ int wc[kCSeries][kCB / 32];
   __shared__ unsigned wb[kCSeries][kCB / 32];
+  __shared__ int boff[kCSeries], btot[kCSeries];
   const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int i = b * kCB + tid;
   const uint32_t m = token_mask(logits, n, batch, i);
   const bool want_union = uidx != nullptr;
+  if (fused) {
+    for (int s = warp; s < kCSeries; s += kCB / 32) {
+      if (!(s < batch || (s == 32 && want_union))) continue;
+      const int* row = scr + (size_t)s * nb;
+      int before = 0, all = 0;
+      for (int q = lane; q < nb; q += 32) {
+        const int v = row[q];
+        all += v;
+        if (q < b) before += v;
+      }
+      before = __reduce_add_sync(0xffffffffu, before);
+      all = __reduce_add_sync(0xffffffffu, all);
+      if (lane == 0) {
+        boff[s] = before;
+        btot[s] = all;
+      }
+    }
+  }
   for (int t = 0; t < batch; ++t) {
     const unsigned bal = __ballot_sync(0xffffffffu, (m >> t) & 1u);
     if (lane == 0) wb[t][warp] = bal;
@@ -939,7 +962,8 @@ __global__ void __launch_bounds__(kCB) cu_write_kernel(const float* logits, int 
   if (lane == 0) wb[32][warp] = bu;
   __syncthreads();
   if (tid < kCSeries) {  // exclusive offsets of the warps, after the blocks before this one
-    int run = (tid < batch || (tid == 32 && want_union)) ? scr[(size_t)tid * nb + b] : 0;
+    const bool on = tid < batch || (tid == 32 && want_union);
+    int run = on ? (fused ? boff[tid] : scr[(size_t)tid * nb + b]) : 0;
     for (int w = 0; w < kCB / 32; ++w) {
       wc[tid][w] = run;
       run += __popc(wb[tid][w]);
@@ -960,11 +984,11 @@ __global__ void __launch_bounds__(kCB) cu_write_kernel(const float* logits, int 
   }
   if (b == nb - 1) {
     if (tid < batch) {
-      const int tot = scr[(size_t)kCSeries * nb + tid];
+      const int tot = fused ? btot[tid] : scr[(size_t)kCSeries * nb + tid];
       cnt[tid] = tot;
       if (tot > cap) set_status(status, PI_ERR_CAPACITY);
     }
-    if (tid == 32 && want_union) *ucnt = scr[(size_t)kCSeries * nb + 32];
+    if (tid == 32 && want_union) *ucnt = fused ? btot[32] : scr[(size_t)kCSeries * nb + 32];
   }
 }
 

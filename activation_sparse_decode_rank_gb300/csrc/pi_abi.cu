@@ -747,11 +747,14 @@ pi_status pi_compact(const float* logits, int32_t n, int32_t batch, int32_t* idx
     int* scr = reinterpret_cast<int*>(static_cast<char*>(ws) + ((ws_bytes - need) & ~(size_t)15));
     const int nb = (n + kCB - 1) / kCB;
     const int wu = union_idx ? 1 : 0;
+    // up to 128 blocks the write kernel sums the counts before it itself
+    const int fused = nb <= 128 ? 1 : 0;
     if (launch_chain(cu_count_kernel, nb, kCB, 0, st, logits, n, batch, wu, scr, nb) !=
             cudaSuccess ||
-        launch_chain(cu_scan_kernel, 1, 1024, 0, st, scr, nb, batch, wu) != cudaSuccess ||
+        (!fused &&
+         launch_chain(cu_scan_kernel, 1, 1024, 0, st, scr, nb, batch, wu) != cudaSuccess) ||
         launch_chain(cu_write_kernel, nb, kCB, 0, st, logits, n, batch, (const int*)scr, nb, idx,
-                     cnt, cap, union_idx, union_cnt, tok_mask, dev_status) != cudaSuccess)
+                     cnt, cap, union_idx, union_cnt, tok_mask, dev_status, fused) != cudaSuccess)
       return PI_ERR_CUDA;
     return PI_OK;
   }
