@@ -177,7 +177,15 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
     // own columns of this job's x: job 0 reads them here; later jobs find
     // them in xo (written by the previous job's R phase)
     if (j == 0 && tid < nq * 8) xo[tid] = __ldcg(sa.x + 8 * q0 + tid);
-    cp_async_wait_group<1>();  // this job's staged Bm columns
+    // independent steps: the whole x of this job goes to shared memory now,
+    // its transfer overlapping stage 1 and the first grid-wide wait (a
+    // chained job's x is complete only after that wait); one copy group in
+    // either case, so the group counts below hold for both
+    if (!sa.chain)
+      for (int i = tid; i < (f.d >> 2); i += kBlock)
+        cp_async16(xs + 4 * i, sa.x + (size_t)j * f.d + 4 * i);
+    cp_async_commit();
+    cp_async_wait_group<2>();  // this job's staged Bm columns (rows, biases and x may still land)
     __syncthreads();
     // U: partial predictor stage 1 over the own columns, u_c[k] for k < r
     if (tid < a.r) {
@@ -215,11 +223,12 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
       bail();
       return;
     }
-    // L: the whole x, u, own logits and list
-    const float* xj = sa.chain ? (j == 0 ? sa.x : sa.y + (size_t)(j - 1) * f.d)
-                               : sa.x + (size_t)j * f.d;
-    for (int i = tid; i < (f.d >> 2); i += kBlock)
-      reinterpret_cast<float4*>(xs)[i] = __ldcg(reinterpret_cast<const float4*>(xj) + i);
+    // L: the whole x (chained), u, own logits and list
+    if (sa.chain) {
+      const float* xj = j == 0 ? sa.x : sa.y + (size_t)(j - 1) * f.d;
+      for (int i = tid; i < (f.d >> 2); i += kBlock)
+        reinterpret_cast<float4*>(xs)[i] = __ldcg(reinterpret_cast<const float4*>(xj) + i);
+    }
     if (tid < f.r) {
       // u[k] from its accumulator; block 0 clears the other buffer (last
       // read by the previous job, before this job's first wait) for the
@@ -230,7 +239,7 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
       }
       if (c == 0) sa.uacc[((size_t)((j + 1) & 1) * f.r + tid) * 16] = 0ull;
     }
-    cp_async_wait_all();  // this job's staged predictor rows and biases
+    cp_async_wait_all();  // this job's staged predictor rows, biases (and x)
     __syncthreads();
     if (compute) own_logits<DT>(a, As, b1s, us, flag, rows);
     __syncthreads();
