@@ -122,6 +122,35 @@ __device__ __noinline__ bool grid_sync(unsigned long long* ctr, unsigned long lo
   return s_ok != 0;
 }
 
+// The two halves of grid_sync, for work between the block's arrival and
+// its wait (work that no other block reads).  grid_arrive: every thread of
+// the block calls it after its writes.  grid_wait: every thread calls it;
+// thread 0 takes the bounded wait of grid_sync.
+__device__ __forceinline__ void grid_arrive(unsigned long long* ctr) {
+  __syncthreads();
+  if (threadIdx.x == 0)
+    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(ctr) : "memory");
+}
+__device__ __noinline__ bool grid_wait(unsigned long long* ctr, unsigned long long target,
+                                       int* status, uint64_t limit_ns) {
+  __shared__ int s_okw;
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    const uint64_t t0 = global_ns();
+    unsigned spins = 0;
+    while ((long long)(ld_acquire64(ctr) - target) < 0) {
+      if ((++spins & 15u) == 0u && global_ns() - t0 > limit_ns) {
+        ok = 0;
+        set_status(status, PI_ERR_TIMEOUT);
+        break;
+      }
+    }
+    s_okw = ok;
+  }
+  __syncthreads();
+  return s_okw != 0;
+}
+
 // ------------------------------------------------------------------ TMA bulk copies
 __device__ __forceinline__ unsigned smem_u32(const void* p) {
   return (unsigned)__cvta_generic_to_shared(p);

@@ -24,10 +24,10 @@
 //      ring: the row-gather GEMV + ReLU and row-axpy of those neurons;
 //   -- wait 2 -- (partial rows written)
 // Right after wait 2, the warps that R leaves idle request the next job's
-// weights that do not depend on its x (the own hot neurons' rows into ring
-// slots, its Bm columns and predictor rows into shared memory, the rest
-// towards L2), so that their transfer overlaps R, U and wait 1 instead of
-// delaying this block's arrival at wait 2.
+// own hot neurons' rows (into ring slots) and Bm columns (into shared
+// memory), so that their transfer overlaps R and U instead of delaying this
+// block's arrival at wait 2; the job's predictor rows and biases are
+// requested by every compute thread once the block has arrived at wait 1.
 // With balancing on (large layers), the blocks publish their cold active
 // neurons after the lists are built and, after one more grid-wide wait, each
 // takes an equal share of them by global rank.
@@ -143,18 +143,25 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
         }
       cp_async_commit();
       for (int k = nh_c + t; k < hot_own; k += nt) prefetch_neuron<GATED>(a, c + k * P);
+    }
+  };
+  // The job's predictor rows (staged, or towards L2) and biases: issued by
+  // every compute thread once the block has arrived at the first grid-wide
+  // wait (they are first read by the logits, after it), one copy group.
+  auto rows_issue = [&]() {
+    if (compute) {
       if (f.a_in_smem) {
         const int rc = a.r >> 3;
-        for (int e = t; e < rows * rc; e += nt) {
+        for (int e = tid; e < rows * rc; e += kThreads) {
           const int jj = e / rc, q = e - jj * rc;
           cp_async16(As + (size_t)jj * f.a_stride + 16 * q,
                      a.A + ((size_t)c + (size_t)jj * P) * a.r + 8 * q);
         }
       } else {
-        for (int jj = t; jj < rows; jj += nt)
+        for (int jj = tid; jj < rows; jj += kThreads)
           prefetch_l2(a.A + ((size_t)c + (size_t)jj * P) * a.r, (size_t)a.r * 2);
       }
-      for (int jj = t; jj < rows; jj += nt) cp_async4(b1s + jj, a.b1 + c + (size_t)jj * P);
+      for (int jj = tid; jj < rows; jj += kThreads) cp_async4(b1s + jj, a.b1 + c + (size_t)jj * P);
       cp_async_commit();
     }
   };
@@ -185,7 +192,7 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
       for (int i = tid; i < (f.d >> 2); i += kBlock)
         cp_async16(xs + 4 * i, sa.x + (size_t)j * f.d + 4 * i);
     cp_async_commit();
-    cp_async_wait_group<2>();  // this job's staged Bm columns (rows, biases and x may still land)
+    cp_async_wait_group<1>();  // this job's staged Bm columns (x may still land)
     __syncthreads();
     // U: partial predictor stage 1 over the own columns, u_c[k] for k < r
     if (tid < a.r) {
@@ -219,7 +226,9 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
                    : "memory");
     }
     ++nbar;
-    if (!grid_sync(f.bar, s_base + nbar * P, f.status, f.limit_ns)) {
+    grid_arrive(f.bar);
+    rows_issue();
+    if (!grid_wait(f.bar, s_base + nbar * P, f.status, f.limit_ns)) {
       bail();
       return;
     }
