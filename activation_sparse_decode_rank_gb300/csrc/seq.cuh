@@ -23,11 +23,12 @@
 //      active list;
 //      ring: the row-gather GEMV + ReLU and row-axpy of those neurons;
 //   -- wait 2 -- (partial rows written)
-// Right after wait 2, the warps that R leaves idle request the next job's
-// own hot neurons' rows (into ring slots) and Bm columns (into shared
-// memory), so that their transfer overlaps R and U instead of delaying this
-// block's arrival at wait 2; the job's predictor rows and biases are
-// requested by every compute thread once the block has arrived at wait 1.
+// Between its arrival at wait 2 and the end of that wait, the block
+// requests the next job's own hot neurons' rows (into ring slots) and Bm
+// columns (into shared memory); the job's predictor rows and biases are
+// requested in the same way at wait 1, and an independent job's x before
+// U.  The transfers overlap the waits and neither delays an arrival nor
+// shares the SM with R.
 // With balancing on (large layers), the blocks publish their cold active
 // neurons after the lists are built and, after one more grid-wide wait, each
 // takes an equal share of them by global rank.
@@ -99,13 +100,12 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
   int nh_c = 0;   // own hot neurons whose rows went to slots for the current job
 
   // The weights of job j that do not depend on its x.  prep_set points the
-  // job's arguments at them; prep_issue requests them: the producer lane
-  // re-arms the ring barriers (no copy may be in flight) and sends the own hot
-  // neurons' rows to their slots; compute threads [t0, t0 + nt) stage the own
-  // Bm columns ([k][q], 16 bytes each, in the last ring slot, a cold one) as
-  // one copy group, then the predictor rows and biases (or prefetch them and
-  // the hot rows beyond the slots towards L2) as a second group, so that
-  // stage 1 waits for the first group only.
+  // job's arguments at them; prep_issue requests the first of them: the
+  // producer lane re-arms the ring barriers (no copy may be in flight) and
+  // sends the own hot neurons' rows to their slots; compute threads
+  // [t0, t0 + nt) stage the own Bm columns ([k][q], 16 bytes each, in the
+  // last ring slot, a cold one) as one copy group and send the hot rows
+  // beyond the slots towards L2.
   bool armed = false;  // the ring barriers hold a previous job's state
   auto prep_set = [&](int j) {
     const SeqLayer& Lw = sa.L[j % sa.R];
@@ -388,7 +388,14 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
       }
     }
     ++nbar;
-    if (!grid_sync(f.bar, s_base + nbar * P, f.status, f.limit_ns)) {
+    grid_arrive(f.bar);
+    // the next job's hot rows and Bm columns, requested while this block
+    // waits (the ring is done and no slot copy is in flight)
+    if (j + 1 < sa.J) {
+      prep_set(j + 1);
+      prep_issue(0, kThreads);
+    }
+    if (!grid_wait(f.bar, s_base + nbar * P, f.status, f.limit_ns)) {
       bail();
       return;
     }
@@ -449,14 +456,6 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
         }
         reinterpret_cast<float4*>(sa.y + (size_t)j * f.d)[col4] = s;
       }
-    }
-    // The next job's weights: the warps past the 2 nq reducing ones arrive
-    // here at once and request them while R runs (no barrier since wait 2);
-    // if every compute warp reduces, all of them do, after R.
-    if (j + 1 < sa.J) {
-      const int t0 = (nq < kSeqMaxQ) ? 64 * nq : 0;
-      prep_set(j + 1);
-      prep_issue(t0, kThreads - t0);
     }
   }
 }
