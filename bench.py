@@ -499,7 +499,9 @@ def run_ours(args):
 
 def run_stack(args):
     """One step = one token through every layer of a residual FFN stack
-    (pi_layer_decode per layer, x_{l+1} = x_l + FFN_l(x_l)).  The layers are
+    (x_{l+1} = x_l + FFN_l(x_l)): one pi_decode_layers launch per token
+    through all layers (engine seq, the default), or pi_layer_decode per
+    layer (engine call).  The layers are
     generated on the GPU (the stack is too large for the host generator to
     make quickly) and packed; the weights of all layers together exceed L2
     many times over, so every layer's weights come from HBM."""
@@ -865,8 +867,8 @@ def main():
     ap.add_argument("--engine", default="auto", choices=["auto", "call", "seq"],
                     help="call: one pi_layer_decode launch per step (per layer); seq: "
                          "pi_decode_layers, one persistent launch per graph-length chunk of "
-                         "steps (per token for a stack); auto: seq for one layer, call for "
-                         "a stack (the faster of the two on each, as measured on GB300)")
+                         "steps (per token for a stack); auto: seq (the faster of the two on "
+                         "one layer and on the 48-layer stack, as measured on GB300)")
     ap.add_argument("--reorder", action="store_true",
                     help="offline profiling + neuron placement timings for --workload")
     ap.add_argument("--sweep", action="store_true",
@@ -882,7 +884,7 @@ def main():
         return run_reorder(args)
     stack = workload_spec(args.workload).get("layers", 1) > 1
     if args.engine == "auto":
-        args.engine = "call" if stack else "seq"
+        args.engine = "seq"
     if stack:
         return run_stack(args)
     return run_ours(args)
