@@ -173,6 +173,68 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
     __syncthreads();
   };
 
+  // R of job jr: own columns of y_jr, one float4 column per compute warp
+  // (warps below 2 nq): lane l sums partials l, l + 32, ... (loads issued
+  // first), then a fixed shuffle tree; + b2 (+ the residual x_jr when
+  // chained, and its columns become the next x's)
+  auto reduce_cols = [&](int jr, const float* b2r) {
+    if (warp < 2 * nq) {
+      const int col4 = 2 * q0 + warp;
+      const float4 bb = b2r ? __ldg(reinterpret_cast<const float4*>(b2r) + col4)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+      constexpr int PU = 6;  // loads in flight per lane (one batch up to 192 blocks)
+      float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int p0 = 0; p0 < P; p0 += 32 * PU) {
+        float4 v[PU];
+#pragma unroll
+        for (int u = 0; u < PU; ++u) {
+          const int p = p0 + lane + 32 * u;
+          v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (p < P) v[u] = __ldcg(reinterpret_cast<const float4*>(f.part + (size_t)p * f.d) + col4);
+        }
+#pragma unroll
+        for (int u = 0; u < PU; ++u) {
+          s.x += v[u].x;
+          s.y += v[u].y;
+          s.z += v[u].z;
+          s.w += v[u].w;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        s.x += __shfl_xor_sync(0xffffffffu, s.x, o);
+        s.y += __shfl_xor_sync(0xffffffffu, s.y, o);
+        s.z += __shfl_xor_sync(0xffffffffu, s.z, o);
+        s.w += __shfl_xor_sync(0xffffffffu, s.w, o);
+      }
+      if (lane == 0) {
+        s.x += bb.x;
+        s.y += bb.y;
+        s.z += bb.z;
+        s.w += bb.w;
+        float4* xo4 = reinterpret_cast<float4*>(xo) + warp;
+        if (sa.chain) {
+          const float4 rr = *xo4;  // x_j at these columns
+          s.x += rr.x;
+          s.y += rr.y;
+          s.z += rr.z;
+          s.w += rr.w;
+          *xo4 = s;  // x_{j+1}
+        }
+        reinterpret_cast<float4*>(sa.y + (size_t)jr * f.d)[col4] = s;
+      }
+    }
+  };
+  // Independent steps, when the warps suffice: job j - 1's column reduce
+  // (warps below 2 nq) runs beside job j's stage 1 (the nU warps after
+  // them), and those warps alone make the block's arrival at wait 1; the
+  // reduce warps join before that wait ends.  Chained steps need the
+  // reduce's columns for stage 1 and keep the two in sequence.
+  const int nU = (f.r + 31) >> 5;
+  const bool ov = !sa.chain && 2 * nq + nU <= kWarps;
+  const int ub = ov ? 64 * nq : 0;  // first stage-1 thread
+  const float* b2prev = nullptr;
+
   if (tid == 0) s_bad = 0;
   prep_set(0);
   prep_issue(0, kThreads);
@@ -194,9 +256,11 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
     cp_async_commit();
     cp_async_wait_group<1>();  // this job's staged Bm columns (x may still land)
     __syncthreads();
+    if (ov && j > 0) reduce_cols(j - 1, b2prev);
     // U: partial predictor stage 1 over the own columns, u_c[k] for k < r
-    if (tid < a.r) {
-      const uint16_t* row = a.Bm + (size_t)tid * f.d + 8 * q0;
+    const int ut = tid - ub;  // k of this thread
+    if (ut >= 0 && ut < a.r) {
+      const uint16_t* row = a.Bm + (size_t)ut * f.d + 8 * q0;
       float acc = 0.f;
       for (int qb = 0; qb < nq; qb += 4) {  // batches of 4 pieces, loads first
         uint4 wv[4];
@@ -204,7 +268,7 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
         for (int t = 0; t < 4; ++t)
           if (qb + t < nq)
             wv[t] = sa.bm_smem
-                        ? *reinterpret_cast<const uint4*>(bms + ((size_t)tid * nq + qb + t) * 16)
+                        ? *reinterpret_cast<const uint4*>(bms + ((size_t)ut * nq + qb + t) * 16)
                         : ld_nc(row + 8 * (qb + t));
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
@@ -221,12 +285,20 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
         acc = 0.f;
       }
       const long long v = __double2ll_rn((double)acc * 4294967296.0);
-      unsigned long long* dst = sa.uacc + ((size_t)(j & 1) * f.r + tid) * 16;
+      unsigned long long* dst = sa.uacc + ((size_t)(j & 1) * f.r + ut) * 16;
       asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(dst), "l"((unsigned long long)v)
                    : "memory");
     }
     ++nbar;
-    grid_arrive(f.bar);
+    if (ov) {  // the stage-1 warps meet, one of them arrives for the block
+      if (ut >= 0 && ut < 32 * nU) {
+        asm volatile("bar.sync 5, %0;" ::"r"(32 * nU) : "memory");
+        if (ut == 0)
+          asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(f.bar) : "memory");
+      }
+    } else {
+      grid_arrive(f.bar);
+    }
     rows_issue();
     if (!grid_wait(f.bar, s_base + nbar * P, f.status, f.limit_ns)) {
       bail();
@@ -408,56 +480,11 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
       sum = __reduce_add_sync(0xffffffffu, sum);
       if (lane == 0) sa.cnt_out[j] = sum;
     }
-    // R: own columns of y_j, one float4 column per compute warp: lane l
-    // sums partials l, l + 32, ... (loads issued first), then a fixed
-    // shuffle tree; + b2 (+ the residual x_j when chained)
-    if (warp < 2 * nq) {
-      const int col4 = 2 * q0 + warp;
-      const float4 bb = b2j ? __ldg(reinterpret_cast<const float4*>(b2j) + col4)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-      constexpr int PU = 6;  // loads in flight per lane (one batch up to 192 blocks)
-      float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int p0 = 0; p0 < P; p0 += 32 * PU) {
-        float4 v[PU];
-#pragma unroll
-        for (int u = 0; u < PU; ++u) {
-          const int p = p0 + lane + 32 * u;
-          v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (p < P) v[u] = __ldcg(reinterpret_cast<const float4*>(f.part + (size_t)p * f.d) + col4);
-        }
-#pragma unroll
-        for (int u = 0; u < PU; ++u) {
-          s.x += v[u].x;
-          s.y += v[u].y;
-          s.z += v[u].z;
-          s.w += v[u].w;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        s.x += __shfl_xor_sync(0xffffffffu, s.x, o);
-        s.y += __shfl_xor_sync(0xffffffffu, s.y, o);
-        s.z += __shfl_xor_sync(0xffffffffu, s.z, o);
-        s.w += __shfl_xor_sync(0xffffffffu, s.w, o);
-      }
-      if (lane == 0) {
-        s.x += bb.x;
-        s.y += bb.y;
-        s.z += bb.z;
-        s.w += bb.w;
-        float4* xo4 = reinterpret_cast<float4*>(xo) + warp;
-        if (sa.chain) {
-          const float4 rr = *xo4;  // x_j at these columns
-          s.x += rr.x;
-          s.y += rr.y;
-          s.z += rr.z;
-          s.w += rr.w;
-          *xo4 = s;  // x_{j+1}
-        }
-        reinterpret_cast<float4*>(sa.y + (size_t)j * f.d)[col4] = s;
-      }
-    }
+    if (!ov) reduce_cols(j, b2j);
+    b2prev = b2j;
   }
+  // independent steps: the last job's column reduce
+  if (ov && warp < 2 * nq) reduce_cols(sa.J - 1, b2prev);
 }
 
 }  // namespace pik

@@ -77,6 +77,17 @@ def test_stack_chain_tiny(packed, balance, monkeypatch):
     assert check_steps(layers, 4, x, True, y, mask, cnt) <= 8
 
 
+@pytest.mark.parametrize("J", [1, 2, 3])
+@pytest.mark.parametrize("chain", [True, False])
+def test_short_launches(J, chain):
+    # independent steps reduce step j - 1 beside step j's stage 1, and the
+    # last step after the loop; the shortest launches cover both ends
+    layers = tiny_layers(2, seed=28)
+    x = synth.gen_x(28, 0, 1 if chain else J, 1024)
+    y, mask, cnt = run_seq(layers, J, x, chain=chain)
+    check_steps(layers, J, x, chain, y, mask, cnt)
+
+
 @pytest.mark.parametrize("chain", [True, False])
 def test_rank_per_layer(chain):
     # each layer its own predictor rank (64, 16, 48, 32): the launch sizes
