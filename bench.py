@@ -867,8 +867,8 @@ def main():
     ap.add_argument("--engine", default="auto", choices=["auto", "call", "seq"],
                     help="call: one pi_layer_decode launch per step (per layer); seq: "
                          "pi_decode_layers, one persistent launch per graph-length chunk of "
-                         "steps (per token for a stack); auto: seq (the faster of the two on "
-                         "one layer and on the 48-layer stack, as measured on GB300)")
+                         "steps (per token for a stack); auto: seq (faster on one layer, "
+                         "the same on the 48-layer stack, as measured on GB300)")
     ap.add_argument("--reorder", action="store_true",
                     help="offline profiling + neuron placement timings for --workload")
     ap.add_argument("--sweep", action="store_true",
