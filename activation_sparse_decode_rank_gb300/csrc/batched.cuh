@@ -115,10 +115,14 @@ __device__ __forceinline__ void split16(float v, uint16_t* hi, uint16_t* lo) {
 // Stage 1 split over the columns: block c of G owns the 8-column chunks
 // [c nch / G, (c+1) nch / G) and writes the partial u of every (token, k),
 // part[c][t][k]; thread k keeps the batch's sums in registers, x's columns
-// of the block are staged in shared memory.
+// of the block are staged in shared memory.  With xhi non-NULL the block
+// also writes the high / low 16-bit parts of its columns of x for the FFN
+// phases ([bp][d], zero rows for padded tokens: the operand split of phase
+// 0, done here while x is at hand).
 template <int DT, int TB>
 __global__ void __launch_bounds__(256) bpu_partial_kernel(const uint16_t* Bm, const float* x, int d,
-                                                          int r, int batch, int G, float* part) {
+                                                          int r, int batch, int G, float* part,
+                                                          uint16_t* xhi, uint16_t* xlo, int bp) {
   pdl_enter();
   extern __shared__ __align__(16) float xs[];  // [batch][w]
   const int c = blockIdx.x, tid = threadIdx.x, nch = d >> 3;
@@ -129,6 +133,16 @@ __global__ void __launch_bounds__(256) bpu_partial_kernel(const uint16_t* Bm, co
     xs[e] = x[(size_t)t * d + 8 * q0 + j];
   }
   __syncthreads();
+  if (xhi) {
+    for (int e = tid; e < bp * w; e += 256) {
+      const int t = e / w, j = e - t * w;
+      uint16_t hi = 0, lo = 0;
+      if (t < batch) split16<DT>(xs[e], &hi, &lo);
+      const size_t o = (size_t)t * d + 8 * q0 + j;
+      xhi[o] = hi;
+      xlo[o] = lo;
+    }
+  }
   for (int k = tid; k < r; k += 256) {
     float acc[TB];
 #pragma unroll

@@ -357,7 +357,7 @@ void bind_weights(FfnArgs& a, const pi_layer_weights& w) {
 pi_status launch_batched(const pi_ffn_desc& D, const pi_layer_weights& w, const float* x,
                          int batch, const int* uidx, const int* ucnt, const uint32_t* tmask,
                          float* y, const float* residual, const WsLayout& L, void* ws,
-                         cudaStream_t st, int32_t* dev_status) {
+                         cudaStream_t st, int32_t* dev_status, bool x_split = false) {
   DevInfo di;
   pi_status s = dev_info(&di);
   if (s != PI_OK) return s;
@@ -393,8 +393,10 @@ pi_status launch_batched(const pi_ffn_desc& D, const pi_layer_weights& w, const 
   const bool bf = D.dtype == PI_BF16;
   const bool m2 = a.bp == 32;
   // phase 0: split x
-  if (launch_chain(bf ? bsplit_x_kernel<1> : bsplit_x_kernel<0>, di.sms * 4, 256, 0, st, a) !=
-      cudaSuccess)
+  // (skipped when the batched predictor of this call already wrote them)
+  if (!x_split &&
+      launch_chain(bf ? bsplit_x_kernel<1> : bsplit_x_kernel<0>, di.sms * 4, 256, 0, st, a) !=
+          cudaSuccess)
     return PI_ERR_CUDA;
   // phase 1
   const int nw = D.gated ? 2 : 1;
@@ -648,9 +650,12 @@ const char* pi_status_string(pi_status s) {
   return "unknown status";
 }
 
-pi_status pi_predict(const pi_ffn_desc* desc, const void* A, const void* Bm, const float* b1,
-                     const float* x, int32_t batch, float* logits, void* ws, size_t ws_bytes,
-                     pi_stream stream) {
+// pi_predict; with split_x (batched calls of pi_layer_decode) the batched
+// stage 1 also writes x's operand parts for the FFN phases and *split is set.
+pi_status predict_impl(const pi_ffn_desc* desc, const void* A, const void* Bm, const float* b1,
+                       const float* x, int32_t batch, float* logits, void* ws, size_t ws_bytes,
+                       pi_stream stream, bool split_x, bool* split) {
+  if (split) *split = false;
   pi_status s = check_desc(desc);
   if (s != PI_OK) return s;
   if (batch < 1 || batch > kMaxBatch) return PI_ERR_SHAPE;
@@ -680,8 +685,12 @@ pi_status pi_predict(const pi_ffn_desc* desc, const void* A, const void* Bm, con
     const bool tb8 = batch <= 8;
     auto fp = bf ? (tb8 ? bpu_partial_kernel<1, 8> : bpu_partial_kernel<1, 32>)
                  : (tb8 ? bpu_partial_kernel<0, 8> : bpu_partial_kernel<0, 32>);
-    if (launch_chain(fp, G, 256, smem1, st, Bh, x, D.d, D.r, batch, G, part) != cudaSuccess)
+    uint16_t* xhi = split_x ? reinterpret_cast<uint16_t*>(b + L.xhi) : nullptr;
+    uint16_t* xlo = split_x ? reinterpret_cast<uint16_t*>(b + L.xlo) : nullptr;
+    if (launch_chain(fp, G, 256, smem1, st, Bh, x, D.d, D.r, batch, G, part, xhi, xlo, L.bp) !=
+        cudaSuccess)
       return PI_ERR_CUDA;
+    if (split) *split = split_x;
     const int bp = L.bp;
     const unsigned gr = (unsigned)((bp * D.r + 31) / 32);
     if (launch_chain(bf ? bpu_reduce_kernel<1> : bpu_reduce_kernel<0>, gr, 256, 0, st,
@@ -728,6 +737,12 @@ pi_status pi_predict(const pi_ffn_desc* desc, const void* A, const void* Bm, con
 #undef PI_L
   if (cudaGetLastError() != cudaSuccess) return PI_ERR_CUDA;
   return PI_OK;
+}
+
+pi_status pi_predict(const pi_ffn_desc* desc, const void* A, const void* Bm, const float* b1,
+                     const float* x, int32_t batch, float* logits, void* ws, size_t ws_bytes,
+                     pi_stream stream) {
+  return predict_impl(desc, A, Bm, b1, x, batch, logits, ws, ws_bytes, stream, false, nullptr);
 }
 
 pi_status pi_compact(const float* logits, int32_t n, int32_t batch, int32_t* idx, int32_t* cnt,
@@ -870,13 +885,15 @@ pi_status pi_layer_decode(const pi_ffn_desc* desc, const pi_layer_weights* w, co
     int32_t* uidx = reinterpret_cast<int32_t*>(b + L.uidx);
     int32_t* ucnt = reinterpret_cast<int32_t*>(b + L.ucnt);
     uint32_t* tmask = reinterpret_cast<uint32_t*>(b + L.tmask);
-    s = pi_predict(desc, w->A, w->Bm, w->b1, x, batch, logits, ws, ws_bytes, stream);
+    bool split = false;  // the predictor also wrote x's operand parts
+    s = predict_impl(desc, w->A, w->Bm, w->b1, x, batch, logits, ws, ws_bytes, stream, true,
+                     &split);
     if (s != PI_OK) return s;
     s = pi_compact(logits, desc->n, batch, idx, cnt, desc->n, uidx, ucnt, tmask, dev_status, ws,
                    ws_bytes, stream);
     if (s != PI_OK) return s;
     return launch_batched(*desc, *w, x, batch, uidx, ucnt, tmask, y, residual, L, ws,
-                          reinterpret_cast<cudaStream_t>(stream), dev_status);
+                          reinterpret_cast<cudaStream_t>(stream), dev_status, split);
   }
   for (int t = 0; t < batch; ++t) {
     FfnArgs a{};
