@@ -27,13 +27,16 @@
 // requests the next job's own hot neurons' rows (into ring slots) and Bm
 // columns (into shared memory); the job's predictor rows and biases are
 // requested in the same way at wait 1, and an independent job's x before
-// U.  The transfers overlap the waits and neither delays an arrival nor
-// shares the SM with R.
+// U.  The transfers overlap the waits and delay no arrival.  Independent
+// jobs also run the previous job's R beside their own U on other warps
+// (when the warps suffice), and only the U warps make the block's arrival
+// at wait 1; chained jobs run R, then U, which needs R's columns.
 // With balancing on (large layers), the blocks publish their cold active
 // neurons after the lists are built and, after one more grid-wide wait, each
 // takes an equal share of them by global rank.
-// A job's x is read only after the previous job is complete: jobs never
-// overlap in anything that depends on their inputs.
+// A job reads its x only after every partial row of the previous job is
+// complete (its wait 2): jobs never overlap in anything that depends on
+// their inputs.
 #pragma once
 
 #include "kernels.cuh"
