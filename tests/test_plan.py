@@ -1,8 +1,9 @@
 """Density / batch-aware dispatch plan (pi_plan_dispatch): host logic, no GPU.
 
 The expected rows are pinned by exact enumeration over every activation
-outcome of a tiny layer; the rest checks the byte counts, the availability
-of each path, the choice of the cheapest estimate and the error channel.
+outcome of a tiny layer and against the union of the oracle's own
+predicted masks; the rest checks the byte counts, the availability of each
+path, the choice of the cheapest estimate and the error channel.
 """
 import itertools
 
@@ -138,3 +139,26 @@ def test_errors():
     L = pi.lib()
     assert L.pi_plan_dispatch(None, 4, None, 0.1, 1, None, out) == pi.PI_ERR_NULL
     assert L.pi_plan_dispatch(desc, 4, None, 0.1, 1, None, None) == pi.PI_ERR_NULL
+
+
+def test_expected_union_matches_the_oracles_masks():
+    # p_i profiled from the oracle's own predicted masks over many tokens;
+    # the plan's expected union of B tokens against the mean union measured
+    # on other tokens of the same layer (tokens are independent, so the
+    # formula holds in expectation; the tolerance covers both samples)
+    import oracle
+    import synth
+    d, n, r = 64, 512, 16
+    L = synth.make_layer(d, n, r, "f16", alpha=0.8, density=0.1, seed=31)
+    prof = np.concatenate([oracle.predict(L, synth.gen_x(31, s, 64, d))[1] > 0
+                           for s in range(64)])
+    p = prof.mean(axis=0).astype(np.float32)  # 4096 tokens
+    desc = pi.make_desc(d, n, r)
+    masks = np.concatenate([oracle.predict(L, synth.gen_x(32, s, 64, d))[1] > 0
+                            for s in range(32)])  # 2048 other tokens
+    for B in (2, 4, 16):
+        groups = masks[: (len(masks) // B) * B].reshape(-1, B, n)
+        unions = groups.any(axis=1).sum(axis=1)
+        _, o = plan(desc, B, p)
+        assert o.union_rows == pytest.approx(unions.mean(), rel=0.03)
+        assert o.active_rows == pytest.approx(masks.sum(axis=1).mean(), rel=0.03)
