@@ -23,7 +23,8 @@ _lock = threading.Lock()
 _lib = None
 
 PI_OK, PI_ERR_NULL, PI_ERR_SHAPE, PI_ERR_DTYPE, PI_ERR_ALIGN, PI_ERR_WORKSPACE, \
-    PI_ERR_CAPACITY, PI_ERR_LAUNCH, PI_ERR_TIMEOUT, PI_ERR_CUDA, PI_ERR_INDEX, PI_ERR_RANGE = range(12)
+    PI_ERR_CAPACITY, PI_ERR_LAUNCH, PI_ERR_TIMEOUT, PI_ERR_CUDA, PI_ERR_INDEX, PI_ERR_RANGE, \
+    PI_ERR_CAPTURE = range(13)
 PI_F16, PI_BF16 = 0, 1
 PI_LAYOUT_SPLIT, PI_LAYOUT_PACKED = 0, 1
 
@@ -99,6 +100,8 @@ SIGNATURES = {
     "pi_layer_decode": (ctypes.c_int, [_DESC, _W, _P, _I32, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "pi_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "pi_selftest_wait_timeout": (ctypes.c_int, [_P, _P, _SZ, _I64, _P]),
+    "pi_selftest_ring_timeout": (ctypes.c_int, [_DESC, _W, _P, _P, _P, _I32, _P, _P, _P, _SZ,
+                                                _I64, _P]),
     "pi_pack_weights": (ctypes.c_int, [_DESC, _P, _P, _P, _P]),
     "pi_layer_decode_static": (ctypes.c_int, [_DESC, _W, _P, _P, _P, _P, _P, _P, _P]),
     "pi_decode_layers": (ctypes.c_int, [_P, _P, _I32, _I32, _P, _I32, _P, _P, _P, _P, _P, _SZ,
@@ -110,6 +113,17 @@ SIGNATURES = {
     "pi_plan_dispatch": (ctypes.c_int, [_DESC, _I32, ctypes.POINTER(ctypes.c_float),
                                         ctypes.c_float, _I32, ctypes.POINTER(pi_cost_model),
                                         ctypes.POINTER(pi_plan)]),
+    "pi_decode_planned": (ctypes.c_int, [_DESC, _W, _I32, _P, _I32, _P, _P, _P, _P, _P, _P, _SZ,
+                                         _P]),
+    "pi_decoder_create": (ctypes.c_int, [_DESC, _W, ctypes.POINTER(ctypes.c_float),
+                                         ctypes.c_float, _I32, ctypes.POINTER(pi_cost_model),
+                                         _P, _P, _P, _P, _P, _SZ, ctypes.POINTER(_P)]),
+    "pi_decoder_run": (ctypes.c_int, [_P, _I32, _P]),
+    "pi_decoder_plan": (ctypes.c_int, [_P, _I32, ctypes.POINTER(pi_plan)]),
+    "pi_decoder_destroy": (None, [_P]),
+    "pi_shard_desc": (ctypes.c_int, [_DESC, _I32, _I32, _DESC]),
+    "pi_shard_layer": (ctypes.c_int, [_DESC, _W, _I32, _I32, _W, _P]),
+    "pi_shard_reduce": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P, _P]),
 }
 
 
@@ -288,3 +302,63 @@ def pi_selftest_wait_timeout(dev_status, ws, limit_ns: int, ws_bytes=None, strea
     return lib().pi_selftest_wait_timeout(_ptr(dev_status), _ptr(ws),
                                           ws.numel() if ws_bytes is None else ws_bytes,
                                           int(limit_ns), _stream(stream))
+
+
+def pi_selftest_ring_timeout(desc, w, x, idx, cnt, cap, y, dev_status, ws, limit_ns: int,
+                             ws_bytes=None, stream=None) -> int:
+    return lib().pi_selftest_ring_timeout(ctypes.byref(desc), ctypes.byref(w), _ptr(x), _ptr(idx),
+                                          _ptr(cnt), cap, _ptr(y), _ptr(dev_status), _ptr(ws),
+                                          ws.numel() if ws_bytes is None else ws_bytes,
+                                          int(limit_ns), _stream(stream))
+
+
+def pi_decode_planned(desc, w, path, x, batch, y, residual, idx_out, cnt_out, dev_status, ws,
+                      ws_bytes=None, stream=None) -> int:
+    return lib().pi_decode_planned(ctypes.byref(desc), ctypes.byref(w), int(path), _ptr(x), batch,
+                                   _ptr(y), _ptr(residual), _ptr(idx_out), _ptr(cnt_out),
+                                   _ptr(dev_status), _ptr(ws),
+                                   ws.numel() if ws_bytes is None else ws_bytes, _stream(stream))
+
+
+def pi_decoder_create(desc, w, p_active, density, allow_dense, model, x, y, residual, dev_status,
+                      ws, ws_bytes=None):
+    """Returns (status, handle); the handle is an opaque int (0 on error).
+    p_active: None or a host float32 numpy array of n values."""
+    pa = None
+    if p_active is not None:
+        import numpy as np
+        arr = np.ascontiguousarray(p_active, dtype=np.float32)
+        pa = arr.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
+    h = ctypes.c_void_p()
+    rc = lib().pi_decoder_create(ctypes.byref(desc), ctypes.byref(w), pa, float(density),
+                                 int(allow_dense),
+                                 ctypes.byref(model) if model is not None else None, _ptr(x),
+                                 _ptr(y), _ptr(residual), _ptr(dev_status), _ptr(ws),
+                                 ws.numel() if ws_bytes is None else ws_bytes, ctypes.byref(h))
+    return rc, (h.value or 0)
+
+
+def pi_decoder_run(dec, batch, stream=None) -> int:
+    return lib().pi_decoder_run(dec, int(batch), _stream(stream))
+
+
+def pi_decoder_plan(dec, batch, out) -> int:
+    return lib().pi_decoder_plan(dec, int(batch), ctypes.byref(out))
+
+
+def pi_decoder_destroy(dec) -> None:
+    lib().pi_decoder_destroy(dec)
+
+
+def pi_shard_desc(desc, G, g, out) -> int:
+    return lib().pi_shard_desc(ctypes.byref(desc), int(G), int(g), ctypes.byref(out))
+
+
+def pi_shard_layer(desc, src, G, g, dst, stream=None) -> int:
+    return lib().pi_shard_layer(ctypes.byref(desc), ctypes.byref(src), int(G), int(g),
+                                ctypes.byref(dst), _stream(stream))
+
+
+def pi_shard_reduce(parts, G, batch, d, residual, y, stream=None) -> int:
+    return lib().pi_shard_reduce(_ptr(parts), int(G), int(batch), int(d), _ptr(residual), _ptr(y),
+                                 _stream(stream))

@@ -54,7 +54,10 @@ struct FfnArgs {
   int* loc_tot;             // [P] active count of each block's own neurons
   unsigned char* mask;      // [n] predicted mask (only when idx_out is wanted)
   float* part;              // [P][d]
-  unsigned long long limit_ns;
+  unsigned long long limit_ns;  // bound of every protocol wait (grid barriers, ring slots)
+  unsigned long long drain_ns;  // bound of the wait for copies already issued to land
+  int skip_issue;               // failure-path self-test only: 1 + the cold entry that the
+                                // producer of every block leaves unissued (0: none)
 };
 
 // ------------------------------------------------------------ async copies
@@ -209,21 +212,38 @@ __device__ void ffn_ring(const FfnArgs& a, const float* xs, const int* lst, cons
   const int c = blockIdx.x;
   const int nc = a.ns - nh;
   const int mc = m - mh;
+  volatile int* vbad = bad;
   if (warp == kWarps) {  // producer warp
     if (lane == 0) {
+      // per cold slot: a copy was issued (bit set in `issued`) and the phase
+      // parity of the latest one (bit of `par`)
+      unsigned issued = 0u, par = 0u;
       for (int kc = 0; kc < mc; ++kc) {
         const int s = nh + kc % nc;
+        if (*vbad) break;  // the compute warps gave up: issue nothing more
         if (kc >= nc &&
             !mbar_wait_sleep(empty + s, (unsigned)((kc / nc - 1) & 1), a.limit_ns)) {
           set_status(a.status, PI_ERR_TIMEOUT);
-          *bad = 1;
+          *vbad = 1;
           break;
         }
+        if (kc + 1 == a.skip_issue) continue;  // self-test: this slot's phase never completes
         issue_neuron<GATED>(a, slots, full, s, lst[mh + kc]);
+        issued |= 1u << (s - nh);
+        par = (par & ~(1u << (s - nh))) | ((unsigned)((kc / nc) & 1) << (s - nh));
       }
+      // every copy issued lands before the slots are re-armed or the block
+      // exits (at once on the normal path: the compute warps consumed them)
+      for (int q = 0; q < nc; ++q)
+        if (((issued >> q) & 1u) &&
+            !mbar_wait_sleep(full + nh + q, (par >> q) & 1u, a.drain_ns)) {
+          set_status(a.status, PI_ERR_TIMEOUT);
+          *vbad = 1;
+        }
     }
     return;
   }
+  __shared__ int s_stop;  // block-uniform decision to abandon the ring
   const unsigned w1b = (GATED ? 4u : 2u) * (unsigned)a.d;
   float xr[NCH][8];
   bool colok[NCH];
@@ -256,9 +276,9 @@ __device__ void ffn_ring(const FfnArgs& a, const float* xs, const int* lst, cons
             cpar ^= 1;
           }
         }
-        if (!mbar_wait(full + sl[q], par, a.limit_ns)) {
+        if (!*vbad && !mbar_wait(full + sl[q], par, a.limit_ns)) {
           set_status(a.status, PI_ERR_TIMEOUT);
-          *bad = 1;
+          *vbad = 1;
         }
       }
     }
@@ -303,7 +323,12 @@ __device__ void ffn_ring(const FfnArgs& a, const float* xs, const int* lst, cons
       if (GATED) h *= s1;
       hb[lane] = h;
     }
+    // a wait of this round (or the producer) gave up: every compute warp
+    // reads the one decision after the barrier and leaves the ring; the
+    // slots are not released, so the producer issues nothing more
+    if (warp == 0 && lane == 0) s_stop = *vbad;
     compute_sync();
+    if (s_stop) break;
     // C: row-axpy of the round's W2 rows
 #pragma unroll
     for (int q = 0; q < kGroup; ++q) {
@@ -557,7 +582,7 @@ __global__ void __launch_bounds__(kBlock, 1) ffn_kernel(const FfnArgs a) {
     if (!grid_sync(a.bar, s_base + (unsigned long long)P, a.status, a.limit_ns)) {
       cp_async_wait_all();
       if (tid == kThreads)
-        for (int j = 0; j < nh_c; ++j) mbar_wait(full + j, 0u, a.limit_ns);
+        for (int j = 0; j < nh_c; ++j) mbar_wait(full + j, 0u, a.drain_ns);
       __syncthreads();
       return;
     }
@@ -657,7 +682,7 @@ __global__ void __launch_bounds__(kBlock, 1) ffn_kernel(const FfnArgs a) {
     for (int j = 0; j < nh_c; ++j) {
       bool used = false;
       for (int k = 0; k < mh; ++k) used |= (lst[k] == c + j * P);
-      if (!used && !mbar_wait(full + j, 0u, a.limit_ns)) set_status(a.status, PI_ERR_TIMEOUT);
+      if (!used && !mbar_wait(full + j, 0u, a.drain_ns)) set_status(a.status, PI_ERR_TIMEOUT);
     }
   }
   if (compute) {

@@ -150,6 +150,14 @@ unsigned long long wait_limit_ns() {
   return g_limit_ns;
 }
 
+// Bounds of a persistent launch's waits: the protocol waits take the
+// process-wide limit; the wait for copies already issued to land takes at
+// least 2 s, so that no block leaves with a copy in flight.
+void set_waits(FfnArgs& a) {
+  a.limit_ns = wait_limit_ns();
+  a.drain_ns = a.limit_ns > 2000000000ull ? a.limit_ns : 2000000000ull;
+}
+
 // How persistent grids are launched.  Default: programmatic dependent
 // launch, which lets a step's weight prefetch overlap the end of the
 // previous step in the same stream; every block is resident because the grid
@@ -295,8 +303,11 @@ int plan_ffn(const pi_ffn_desc& D, int mode, int P, int positions, int smem_limi
   return fixed + ns * a.slot_bytes;
 }
 
+// limit_ns / skip_issue: the failure-path self-test's shorter protocol
+// bound and unissued entry (0: the process-wide bound, none).
 template <int MODE>
-pi_status launch_ffn(const pi_ffn_desc& D, FfnArgs& a, int positions, cudaStream_t st) {
+pi_status launch_ffn(const pi_ffn_desc& D, FfnArgs& a, int positions, cudaStream_t st,
+                     unsigned long long limit_ns = 0, int skip_issue = 0) {
   DevInfo di;
   pi_status s = dev_info(&di);
   if (s != PI_OK) return s;
@@ -308,7 +319,9 @@ pi_status launch_ffn(const pi_ffn_desc& D, FfnArgs& a, int positions, cudaStream
   if (smem == 0 || a.grp < 1) return PI_ERR_SHAPE;
   s = ensure_smem(reinterpret_cast<const void*>(fn), smem);
   if (s != PI_OK) return s;
-  a.limit_ns = wait_limit_ns();
+  set_waits(a);
+  if (limit_ns) a.limit_ns = limit_ns;
+  a.skip_issue = skip_issue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)P);
   cfg.blockDim = dim3(kBlock);
@@ -462,13 +475,18 @@ static __device__ __align__(256) unsigned char g_static_scratch[PI_STATIC_SCRATC
 std::unordered_map<int, void*> g_static_ptr;  // device -> address of g_static_scratch
 
 // Device address of g_static_scratch on the current device, looked up once
-// per device (host code only has a stand-in for the symbol).
-pi_status static_scratch(void** out) {
+// per device (host code only has a stand-in for the symbol).  The lookup
+// is refused while `st` is being captured into a graph (the capture would
+// be invalidated); later calls on the device only read the cached address.
+pi_status static_scratch(void** out, cudaStream_t st) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PI_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
   auto it = g_static_ptr.find(dev);
   if (it == g_static_ptr.end()) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return PI_ERR_CUDA;
+    if (cs != cudaStreamCaptureStatusNone) return PI_ERR_CAPTURE;
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) return PI_ERR_CUDA;
     it = g_static_ptr.emplace(dev, p).first;
@@ -477,7 +495,10 @@ pi_status static_scratch(void** out) {
   return PI_OK;
 }
 
-// Regions of the fused batch-1 kernel's scratch with exactly P partial rows.
+// Regions of the fused batch-1 kernel's scratch with exactly P partial rows:
+// the barrier block, the predictor partials (r x kSMax), the per-block
+// counts, the n-byte mask and the P x d partial outputs, each rounded up to
+// 256 bytes.
 WsLayout static_layout(const pi_ffn_desc& D, int P) {
   WsLayout L{};
   size_t off = 0;
@@ -487,15 +508,41 @@ WsLayout static_layout(const pi_ffn_desc& D, int P) {
     return o;
   };
   L.ctrl = take(256);
-  // predictor partials: r x kSMax (one-layer kernel) or r x P (sequence kernel)
-  L.upart = take(sizeof(float) * (size_t)D.r * (kPMax > kSMax ? kPMax : kSMax));
+  L.upart = take(sizeof(float) * (size_t)D.r * kSMax);
   L.loc_tot = take(sizeof(int) * (size_t)P);
   L.mask = take((size_t)D.n);
   L.part = take(sizeof(float) * (size_t)P * D.d);
   L.u = L.logits = 0;
-  L.cscr = take(compact_scratch_bytes(D.n));
   L.total = off;
   return L;
+}
+
+// Batch-1 sparse FFN over a caller's active list (the body of pi_sparse_ffn
+// for batch 1, and of its failure-path self-test).
+pi_status sparse_one(const pi_ffn_desc* desc, const pi_layer_weights* w, const float* x,
+                     const int32_t* idx, const int32_t* cnt, int32_t cap, float* y,
+                     int32_t* dev_status, void* ws, size_t ws_bytes, pi_stream stream,
+                     unsigned long long limit_ns, int skip_issue) {
+  if (!x || !y || !idx || !cnt || !dev_status || !ws) return PI_ERR_NULL;
+  const void* ps[] = {x, y, idx, cnt, dev_status, ws};
+  for (const void* p : ps)
+    if (!aligned16(p)) return PI_ERR_ALIGN;
+  if (cap < 0) return PI_ERR_SHAPE;
+  const WsLayout L = ws_layout(*desc, 1);
+  if (ws_bytes < L.total) return PI_ERR_WORKSPACE;
+  FfnArgs a{};
+  bind_weights(a, *w);
+  bind_ws(a, L, ws);
+  a.x = x;
+  a.residual = nullptr;
+  a.y = y;
+  a.idx_in = idx;
+  a.cnt_in = cnt;
+  a.cap = cap;
+  a.status = dev_status;
+  const int positions = cap < desc->n ? cap : desc->n;
+  return launch_ffn<kSparse>(*desc, a, positions > 0 ? positions : 1,
+                             reinterpret_cast<cudaStream_t>(stream), limit_ns, skip_issue);
 }
 
 }  // namespace
@@ -524,16 +571,18 @@ pi_status pi_layer_decode_static(const pi_ffn_desc* desc, const pi_layer_weights
   const void* ps[] = {x, y, residual, idx_out, cnt_out, dev_status};
   for (const void* p : ps)
     if (p && !aligned16(p)) return PI_ERR_ALIGN;
+  // a shape too large even for a one-block grid is refused before any CUDA call
+  if (static_layout(*desc, 1).total > PI_STATIC_SCRATCH_BYTES) return PI_ERR_WORKSPACE;
   DevInfo di;
   s = dev_info(&di);
   if (s != PI_OK) return s;
   const int P = di.sms < kPMax ? di.sms : kPMax;
   const WsLayout L = static_layout(*desc, P);
   if (L.total > PI_STATIC_SCRATCH_BYTES) return PI_ERR_WORKSPACE;
-  void* scratch = nullptr;
-  s = static_scratch(&scratch);
-  if (s != PI_OK) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  void* scratch = nullptr;
+  s = static_scratch(&scratch, st);
+  if (s != PI_OK) return s;
   if (cudaMemsetAsync(static_cast<char*>(scratch) + L.ctrl, 0, 256, st) != cudaSuccess)
     return PI_ERR_CUDA;
   FfnArgs a{};
@@ -646,6 +695,8 @@ const char* pi_status_string(pi_status s) {
     case PI_ERR_CUDA: return "a CUDA runtime call failed";
     case PI_ERR_INDEX: return "an active-list entry is outside [0, n)";
     case PI_ERR_RANGE: return "a predictor partial sum is outside the fixed-point range";
+    case PI_ERR_CAPTURE:
+      return "a one-time setup of this call cannot run while the stream is being captured";
   }
   return "unknown status";
 }
@@ -807,26 +858,7 @@ pi_status pi_sparse_ffn(const pi_ffn_desc* desc, const pi_layer_weights* w, cons
     return launch_batched(*desc, *w, x, batch, union_idx, union_cnt, tok_mask, y, nullptr, L, ws,
                           reinterpret_cast<cudaStream_t>(stream), dev_status);
   }
-  if (!x || !y || !idx || !cnt || !dev_status || !ws) return PI_ERR_NULL;
-  const void* ps[] = {x, y, idx, cnt, dev_status, ws};
-  for (const void* p : ps)
-    if (!aligned16(p)) return PI_ERR_ALIGN;
-  if (cap < 0) return PI_ERR_SHAPE;
-  const WsLayout L = ws_layout(*desc, batch);
-  if (ws_bytes < L.total) return PI_ERR_WORKSPACE;
-  FfnArgs a{};
-  bind_weights(a, *w);
-  bind_ws(a, L, ws);
-  a.x = x;
-  a.residual = nullptr;
-  a.y = y;
-  a.idx_in = idx;
-  a.cnt_in = cnt;
-  a.cap = cap;
-  a.status = dev_status;
-  const int positions = cap < desc->n ? cap : desc->n;
-  return launch_ffn<kSparse>(*desc, a, positions > 0 ? positions : 1,
-                             reinterpret_cast<cudaStream_t>(stream));
+  return sparse_one(desc, w, x, idx, cnt, cap, y, dev_status, ws, ws_bytes, stream, 0, 0);
 }
 
 pi_status pi_dense_ffn(const pi_ffn_desc* desc, const pi_layer_weights* w, const float* x,
@@ -958,7 +990,7 @@ pi_status pi_decode_layers(const pi_ffn_desc* descs, const pi_layer_weights* lay
   a.idx_out = nullptr;
   a.cnt_out = nullptr;
   a.status = dev_status;
-  a.limit_ns = wait_limit_ns();
+  set_waits(a);
   SeqArgs sa{};
   sa.f = a;
   sa.J = J;
@@ -1092,6 +1124,19 @@ pi_status pi_pack_weights(const pi_ffn_desc* desc, const void* W1, const void* W
   return PI_OK;
 }
 
+pi_status pi_selftest_ring_timeout(const pi_ffn_desc* desc, const pi_layer_weights* w,
+                                   const float* x, const int32_t* idx, const int32_t* cnt,
+                                   int32_t cap, float* y, int32_t* dev_status, void* ws,
+                                   size_t ws_bytes, int64_t limit_ns, pi_stream stream) {
+  pi_status s = check_desc(desc);
+  if (s != PI_OK) return s;
+  s = check_weights(*desc, w, false);
+  if (s != PI_OK) return s;
+  if (limit_ns < 1000 || limit_ns > 5000000000LL) return PI_ERR_SHAPE;
+  return sparse_one(desc, w, x, idx, cnt, cap, y, dev_status, ws, ws_bytes, stream,
+                    (unsigned long long)limit_ns, 1);
+}
+
 pi_status pi_selftest_wait_timeout(int32_t* dev_status, void* ws, size_t ws_bytes,
                                    int64_t limit_ns, pi_stream stream) {
   if (!dev_status || !ws) return PI_ERR_NULL;
@@ -1105,3 +1150,6 @@ pi_status pi_selftest_wait_timeout(int32_t* dev_status, void* ws, size_t ws_byte
 }
 
 }  // extern "C"
+
+#include "decoder.cuh"
+#include "shard.cuh"

@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
   auto bail = [&]() {
     cp_async_wait_all();
     if (tid == kThreads)
-      for (int k = 0; k < nh_c; ++k) mbar_wait(full + k, 0u, f.limit_ns);
+      for (int k = 0; k < nh_c; ++k) mbar_wait(full + k, 0u, f.drain_ns);
     __syncthreads();
   };
 
@@ -445,11 +445,16 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
       for (int k = 0; k < nh_c; ++k) {
         bool used = false;
         for (int e = 0; e < mh; ++e) used |= (lst[e] == c + k * P);
-        if (!used && !mbar_wait(full + k, 0u, f.limit_ns)) set_status(f.status, PI_ERR_TIMEOUT);
+        if (!used && !mbar_wait(full + k, 0u, f.drain_ns)) set_status(f.status, PI_ERR_TIMEOUT);
       }
     }
     nh_c = 0;  // every slot copy of this job has landed
     __syncthreads();
+    if (s_bad) {  // a ring wait gave up (block-uniform after the barrier)
+      cp_async_wait_all();
+      __syncthreads();
+      return;
+    }
     const float* b2j = a.b2;
     if (compute) {  // the partial rows go out first: wait 2 fences them
 #pragma unroll

@@ -1,20 +1,24 @@
 """Decode benchmark of the activation-sparse FFN on GB300.
 
-One step = one batch-1 decode step of one FFN layer through pi_layer_decode
-(predictor, compaction, row-gather GEMV + ReLU, row-axpy down projection,
-deterministic split reduction: one persistent kernel launch).  The default
-workload is the OPT-6.7B-shaped FFN (d=4096, n=16384, r=128, fp16 weights,
-Zipf(0.9) activation profile at 6 % mean density), seeded and synthetic.
+Default workload: the OPT-30B-shaped 48-layer FFN stack (d = 7168,
+n = 28672, r = 256 per layer, fp16 weights, residual adds, per-layer Zipf
+activation profiles at 3-15 % density; about 39 GB of weights resident in
+HBM), seeded and synthetic.  One step = one token decoded at batch 1
+through all 48 layers (predictor, compaction, row-gather GEMV + ReLU,
+row-axpy down projection, fixed-order reduction, residual add per layer):
+one pi_decode_layers launch.  The stack exceeds the L2 cache hundreds of
+times over, so every layer's weights come from HBM.
 
-Each step reads a different copy of the layer's weights (rotating
-replicas whose total is several times the L2 size), so every step's
-weights come from HBM; x is fresh per step.  Steps run as CUDA-graph
-replays; timing uses CUDA events on the launching stream.
+Single-layer workloads (--workload ...) run the same engine with rotating
+weight replicas larger than L2.  Steps run as CUDA-graph replays; each
+timed region is K steps bracketed by a barrier and device synchronisation,
+timed with CUDA events on the launching stream, repeated and reported as
+the median.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference]
 
 Under torchrun (N > 1) every rank decodes its own token stream on its own
-GPU (replicas only: the path has no exchange step); rank 0 prints the
+GPU (replicas only: each rank holds the whole model); rank 0 prints the
 aggregate.
 """
 from __future__ import annotations
@@ -37,7 +41,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "sparse-FFN decode tokens/s at batch 1; achieved HBM GB/s vs peak (active bytes)"
-DEFAULT_WORKLOAD = "opt6.7b_ffn_d4096_n16384_r128_f16"
+DEFAULT_WORKLOAD = "opt30b_ffn_stack_48x_d7168_n28672_r256_f16"
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -85,8 +89,9 @@ def measured_peaks():
 
 
 def stored_traffic(kernel_key):
-    """dram bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source; else None."""
+    """The committed ncu figure for a kernel and workload, if it was taken on
+    the current kernel source: (DRAM bytes per decode step, the algorithmic
+    bytes per step of that capture); else None."""
     if not os.path.exists(PROFILE_TRAFFIC):
         return None
     try:
@@ -96,7 +101,9 @@ def stored_traffic(kernel_key):
     e = j.get(kernel_key)
     if not e or e.get("csrc_hash") != csrc_hash():
         return None
-    return e.get("dram_bytes_per_launch")
+    if "dram_bytes_per_step" not in e:
+        return None
+    return float(e["dram_bytes_per_step"]), float(e.get("algorithmic_bytes_per_step", 0.0))
 
 
 class ClockSampler:
@@ -155,6 +162,28 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def timed_regions(torch, stream, fn, repeats, barrier):
+    """Runs fn() (which enqueues one timed region of work on `stream`)
+    `repeats` times, each bracketed by a barrier and device synchronisation
+    and timed with CUDA events on the stream; returns the milliseconds of
+    each region."""
+    out = []
+    for _ in range(repeats):
+        barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        stream.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        out.append(e0.elapsed_time(e1))
+    return out
+
+
 # ------------------------------------------------------------------ workload
 def workload_spec(name):
     from synth.workloads import WORKLOADS
@@ -169,6 +198,33 @@ def hot_prefix_len(w):
     c = synth.zipf_calibrate(w["n"], w["alpha"], w["density"])
     p = synth.zipf_probs(w["n"], w["alpha"], c)
     return int((p >= 0.5).sum())
+
+
+def layer_config(w, args, hot, R, layer_bytes, step_bytes_est, l2):
+    """The `config` of a single-layer line (shared by both arms)."""
+    return {
+        "workload": args.workload, "batch": 1, "weights": w["dtype"], "density": w["density"],
+        "d": w["d"], "n": w["n"], "r": w["r"], "gated": bool(w["gated"]), "hot_prefix": hot,
+        "layout": args.layout,
+        "l2": (f"inputs larger than L2: {R} rotating weight replicas "
+               f"({R * layer_bytes / 1e9:.1f} GB; each step reads its own copy)"
+               if R * step_bytes_est >= 3 * l2 else
+               f"L2-warm (not HBM-bound): {R} weight replica(s) of "
+               f"{layer_bytes / 1e9:.2f} GB reused across steps"),
+        "parallelism": "single GPU",
+    }
+
+
+def stack_config(w, L):
+    """The `config` of a stack line (shared by both arms)."""
+    d, n, r = w["d"], w["n"], w["r"]
+    return {"workload": w["name"], "batch": 1, "layers": L, "weights": w["dtype"],
+            "d": d, "n": n, "r": r, "gated": False, "layout": "packed",
+            "hot_prefix": "per layer: neurons with p_i >= 0.5",
+            "density": "per layer 3-15 % (Zipf alpha_l ~ U[0.7, 1.2])",
+            "l2": f"inputs larger than L2: {L} distinct layers resident "
+                  f"({L * (n * 2 * d * 2 + n * r * 2 + r * d * 2) / 1e9:.1f} GB)",
+            "parallelism": "single GPU"}
 
 
 def cpu_oracle_sample(w, budget_s, max_tokens, warm=3):
@@ -195,26 +251,117 @@ def cpu_oracle_sample(w, budget_s, max_tokens, warm=3):
     return done, spent, oracle.get_threads()
 
 
+# ------------------------------------------------------------------ the stack's layers
+def build_stack(w, dev, L):
+    """The first L layers of the residual stack, generated on the GPU and
+    packed (one [W1 row | W2 row] record per neuron).  Returns descriptors,
+    weight structs, the tensors that hold them and the predictor bytes."""
+    import torch
+
+    import activation_sparse_decode_rank_gb300 as pi
+    import synth
+    d, n, r = w["d"], w["n"], w["r"]
+    alpha, rho, cz, scale = synth.stack_plan(w["seed"], w["layers"], n)
+    descs, wts, keep, pred_bytes = [], [], [], 0
+    for l in range(L):
+        g = synth.make_layer_gpu(d, n, r, w["dtype"], alpha=float(alpha[l]), zipf_c=float(cz[l]),
+                                 seed=w["seed"], layer=l, bias_scale=float(scale[l]), device=dev)
+        p = synth.zipf_probs(n, float(alpha[l]), float(cz[l]))
+        hot = int((p >= 0.5).sum())
+        desc = pi.make_desc(d, n, r, w["dtype"], False, hot, packed=True)
+        rec = torch.empty((n, 2 * d), dtype=torch.int16, device=dev)
+        pi.check(pi.pi_pack_weights(desc, g["W1"], g["W2"], rec), "pi_pack_weights")
+        torch.cuda.synchronize()
+        del g["W1"], g["W2"]
+        keep.append((g, rec))
+        descs.append(desc)
+        wts.append(pi.make_weights(g["A"], g["Bm"], g["b1"], rec, None, g["b2"]))
+        pred_bytes += n * r * 2 + r * d * 2 + n * 4
+    torch.cuda.empty_cache()
+    return descs, wts, keep, pred_bytes
+
+
+def host_layer(w, g, rec):
+    """Host copy of one packed GPU layer in the oracle's split form."""
+    import synth
+    d = w["d"]
+    cpu = lambda t: t.cpu().numpy()
+    R = cpu(rec).view(np.uint16)
+    return synth.Layer(d, w["n"], w["r"], w["dtype"], False, cpu(g["A"]).view(np.uint16),
+                       cpu(g["Bm"]).view(np.uint16), cpu(g["b1"]),
+                       np.ascontiguousarray(R[:, :d]), np.ascontiguousarray(R[:, d:]),
+                       cpu(g["b2"]), {})
+
+
+def stack_oracle_sample(w, keep, tokens, warm, budget_s, seed_off=0):
+    """Times the fp64 oracle on the host cores through every layer of the
+    stack, token by token: x_{l+1} = x_l + FFN_l(x_l) with predict, compact
+    and the sparse FFN per layer, the residual stream kept in fp32.  Layers
+    are visited one at a time (each copied to the host once, outside the
+    timed part); `warm` untimed tokens go first.  If layer 0 shows that
+    `tokens` would exceed budget_s of oracle time, the sample keeps the
+    first tokens that fit.  Returns (timed tokens, seconds, threads)."""
+    import oracle
+    import synth
+    d = w["d"]
+    L = len(keep)
+    xs = [synth.gen_x(w["seed"] + seed_off, s, 1, d)[0].astype(np.float32)
+          for s in range(warm + tokens)]
+    spent = [0.0] * (warm + tokens)
+    keep_n = warm + tokens
+    for l, (g, rec) in enumerate(keep):
+        H = host_layer(w, g, rec)
+        for t in range(keep_n):
+            t0 = time.perf_counter()
+            _, _, _, xn = oracle.layer_decode(H, xs[t], residual=True)
+            spent[t] += time.perf_counter() - t0
+            xs[t] = xn
+        del H
+        if l == 0 and tokens > 1:
+            per_tok = sum(spent[warm:keep_n]) / tokens * L
+            fit = max(1, int(budget_s / per_tok)) if per_tok > 0 else tokens
+            keep_n = warm + min(tokens, fit)
+    done = keep_n - warm
+    return done, sum(spent[warm:keep_n]), oracle.get_threads()
+
+
 # ------------------------------------------------------------------ reference arm
 def run_reference(args):
-    rank, world, _ = dist_env()
+    """The oracle as the reference arm: the same workload, config, steps and
+    warm-up as our arm, timed on the host cores (rank 0 only)."""
+    rank, world, local = dist_env()
     if rank != 0:
         return 0
     w = workload_spec(args.workload)
+    w["name"] = args.workload
+    budget = float(os.environ.get("PI_REF_BUDGET_S", "120"))
     if w.get("layers", 1) > 1:
-        raise SystemExit("bench: the reference arm times single-layer workloads")
-    budget = float(os.environ.get("PI_REF_BUDGET_S", "30"))
-    warm = min(args.warmup, 3)
-    done, dt, cores = cpu_oracle_sample(w, budget_s=budget, max_tokens=args.steps, warm=warm)
+        import torch
+        dev = torch.device("cuda", local)
+        torch.cuda.set_device(dev)
+        L = args.layers if args.layers > 0 else w["layers"]
+        # the synthetic weights come from the GPU generator (input generation
+        # only, untimed; the host generator would take minutes per layer)
+        _, _, keep, _ = build_stack(w, dev, L)
+        done, dt, cores = stack_oracle_sample(w, keep, args.steps, args.warmup, budget)
+        config = stack_config(w, L)
+        sample = (f"{done} of {args.steps} requested tokens (after {args.warmup} untimed) "
+                  f"through all {L} layers of {args.workload}, fp64 oracle predict+compact+"
+                  f"sparse FFN + residual per layer, on {cores} host threads")
+    else:
+        done, dt, cores = cpu_oracle_sample(w, budget_s=budget, max_tokens=args.steps,
+                                            warm=args.warmup)
+        hot = hot_prefix_len(w) if args.hot < 0 else args.hot
+        config = layer_config(w, args, hot, 0, 0, 0, 1)
+        config.pop("l2")
+        sample = (f"{done} of {args.steps} requested decode steps of {args.workload} "
+                  f"(time-bounded at {budget:.0f} s), fp64 oracle on {cores} host threads")
     v = done / dt
-    sample = (f"{done} of {args.steps} requested decode steps of {args.workload} "
-              f"(time-bounded at {budget:.0f} s), fp64 oracle on {cores} host threads")
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
-        "n_gpus": world, "steps": done, "warmup": warm, "ms_per_step": dt / done * 1e3,
+        "n_gpus": world, "steps": done, "warmup": args.warmup, "ms_per_step": dt / done * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic",
-        "config": {"workload": args.workload, "batch": 1, "density": w["density"]},
+        "data": "synthetic", "config": config,
         "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -224,7 +371,7 @@ def run_reference(args):
     return 0
 
 
-# ------------------------------------------------------------------ our arm
+# ------------------------------------------------------------------ our arm: one layer
 def run_ours(args):
     import torch
 
@@ -258,6 +405,7 @@ def run_ours(args):
     pred_bytes = n * r * 2 + r * d * 2 + n * 4
     step_bytes_est = pred_bytes + w["density"] * n * m_rows * d * 2
     R = args.replicas if args.replicas > 0 else max(2, math.ceil(3 * l2 / step_bytes_est))
+    R = min(R, 128)
     desc = pi.make_desc(d, n, r, w["dtype"], gated, hot, packed=args.layout == "packed")
     base = [up(L.A), up(L.Bm), up(L.b1), up(L.W1), up(L.W2), up(L.b2)]
     if args.layout == "packed":
@@ -268,172 +416,127 @@ def run_ours(args):
     reps = [base] + [[t.clone() if t is not None else None for t in base] for _ in range(R - 1)]
     layer_bytes = sum(t.numel() * t.element_size() for t in base if t is not None)
     wts = [pi.make_weights(*rp) for rp in reps]
+    descs = [desc] * R
 
-    G = min(args.steps, args.graph_len)
+    K = args.steps
+    # one pi_decode_layers launch decodes G steps (independent tokens, each
+    # read only after the previous step is complete); K is a multiple of G
+    G = min(K, args.graph_len)
+    if K % G:
+        raise SystemExit(f"bench: --steps must be a multiple of the steps per launch {G}")
     xs = torch.from_numpy(np.concatenate(
         [synth.gen_x(w["seed"] + 1000 * rank, s, 1, d) for s in range(G)])).to(dev)
-    y = torch.empty((1, d), dtype=torch.float32, device=dev)
-    cnts = torch.zeros((G, 4), dtype=torch.int32, device=dev)  # 16-byte rows
+    ys = torch.empty((G, d), dtype=torch.float32, device=dev)
+    cseq = torch.zeros((G + 4,), dtype=torch.int32, device=dev)
     st = torch.zeros(4, dtype=torch.int32, device=dev)
     ws = pi.workspace(desc, 1, dev)
     stream = torch.cuda.Stream(device=dev)
 
-    seq = args.engine == "seq"
-    if seq:
-        R = min(R, 128)
-        wts = wts[:R]
-        ys = torch.empty((G, d), dtype=torch.float32, device=dev)
-        cseq = torch.zeros((G + 4,), dtype=torch.int32, device=dev)
-    steps_per_call = G if seq else 1
+    def launch(J, xsrc, ydst, cnt):
+        pi.check(pi.pi_decode_layers(descs, wts, J, xsrc, 0, ydst, cnt, None, st, ws,
+                                     stream=stream), "pi_decode_layers")
 
-    def step(s, cnt_slot=True, wt=None, xsrc=None, ydst=None):
-        if seq:  # s counts calls; each call decodes G steps in one launch
-            rc = pi.pi_decode_layers([desc] * R, wts, G, xs if xsrc is None else xsrc, 0,
-                                     ys if ydst is None else ydst, cseq if cnt_slot else None,
-                                     None, st, ws, stream=stream)
-            pi.check(rc, "pi_decode_layers")
-            return
-        rc = pi.pi_layer_decode(desc, wts[s % R] if wt is None else wt,
-                                xs[s % G] if xsrc is None else xsrc, 1,
-                                y if ydst is None else ydst, None, None,
-                                cnts[s % G] if cnt_slot else None, st, ws, stream=stream)
-        pi.check(rc, "pi_layer_decode")
-
-    def capture(nsteps, fn):
+    def capture(fn):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
             with torch.cuda.graph(g, stream=stream):
-                for s in range(nsteps):
-                    fn(s)
+                fn()
         return g
 
-    if seq and args.steps % G:
-        raise SystemExit(f"bench: --steps must be a multiple of the graph length {G} (seq engine)")
     with torch.cuda.stream(stream):
-        for s in range(1 if seq else min(G, 8)):   # eager run first: attribute setup, sanity
-            step(s)
+        launch(G, xs, ys, cseq)  # eager run first: attribute setup, sanity
         stream.synchronize()
-        if int(st[0]) != 0:
-            raise SystemExit(f"bench: device status {pi.status_string(int(st[0]))}")
-    calls_per_graph = 1 if seq else G
-    g_main = capture(calls_per_graph, step)
-    tail = 0 if seq else args.steps % G
-    g_tail = capture(tail, step) if tail else None
-    g_warm = g_main if seq else capture(min(args.warmup, G), step)
-
-    def replay_steps(k):
-        full, rem = divmod(k, G)
-        for _ in range(full):
-            g_main.replay()
-        if rem:
-            g_tail.replay()
+    if int(st[0]) != 0:
+        raise SystemExit(f"bench: device status {pi.status_string(int(st[0]))}")
+    launches_per_region = K // G
+    g_main = capture(lambda: [launch(G, xs, ys, cseq) for _ in range(launches_per_region)])
 
     def barrier():
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
 
-    # warmup (untimed): at least W steps
-    with torch.cuda.stream(stream):
-        gw = G if seq else min(args.warmup, G)
-        for _ in range(math.ceil(args.warmup / gw)):
-            g_warm.replay()
+    with torch.cuda.stream(stream):  # warm-up (untimed): at least W steps
+        for _ in range(max(1, math.ceil(args.warmup / K))):
+            g_main.replay()
         stream.synchronize()
-    barrier()
-    torch.cuda.synchronize()
 
     sampler = ClockSampler(local)
     sampler.start()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        replay_steps(args.steps)
-        e1.record(stream)
-    stream.synchronize()
-    barrier()
-    torch.cuda.synchronize()
+    regions = timed_regions(torch, stream, g_main.replay, args.repeats, barrier)
     clocks = sampler.stop()
-    ms = e0.elapsed_time(e1)
     if int(st[0]) != 0:
         raise SystemExit(f"bench: device status {pi.status_string(int(st[0]))}")
+    ms = statistics.median(regions)
 
     # byte accounting from the run's own active counts
-    cnt_host = (cseq[:G] if seq else cnts[:, 0]).cpu().numpy().astype(np.float64)
+    cnt_host = cseq[:G].cpu().numpy().astype(np.float64)
     mean_cnt = float(cnt_host.mean())
     active_bytes = mean_cnt * m_rows * d * 2
     alg_bytes = pred_bytes + active_bytes
 
-    # max over ranks
-    value, t_max = aggregate([max_over_ranks(ms, world, dev)], [args.steps * world], world)
-    ms_per_step = t_max / args.steps
-    launches = args.steps // steps_per_call
-    per_launch_s = ms / launches / 1e3
+    value, t_max = aggregate([max_over_ranks(ms, world, dev)], [K * world], world)
+    ms_per_step = t_max / K
+    per_launch_s = ms / launches_per_region / 1e3
     peak, peak_kind = measured_peaks()
-    achieved = alg_bytes * steps_per_call / per_launch_s / 1e9
+    achieved = alg_bytes * G / per_launch_s / 1e9
+    tr = stored_traffic(f"seq_kernel:{args.workload}")
+    traffic = tr[0] * G if tr else None  # DRAM bytes of one launch of G steps
 
-    # dense-FFN comparison point (same replicas, same protocol)
-    dense_steps = min(200, args.steps)
+    # dense-FFN comparison point (same replicas, one launch per step)
+    dense_steps = 200
     ws_d = pi.workspace(desc, 1, dev)
+    y1 = torch.empty((1, d), dtype=torch.float32, device=dev)
 
-    def dstep(s):
-        pi.check(pi.pi_dense_ffn(desc, wts[s % R], xs[s % G], 1, y, ws_d, stream=stream))
+    def dense_all():
+        for s in range(dense_steps):
+            pi.check(pi.pi_dense_ffn(desc, wts[s % R], xs[s % G], 1, y1, ws_d, stream=stream))
 
     with torch.cuda.stream(stream):
         for s in range(2):
-            dstep(s)
-    g_dense = capture(dense_steps, dstep)
+            pi.check(pi.pi_dense_ffn(desc, wts[s % R], xs[s % G], 1, y1, ws_d, stream=stream))
+    g_dense = capture(dense_all)
     with torch.cuda.stream(stream):
         g_dense.replay()
-        d0 = torch.cuda.Event(enable_timing=True)
-        d1 = torch.cuda.Event(enable_timing=True)
-        d0.record(stream)
-        g_dense.replay()
-        d1.record(stream)
-    stream.synchronize()
-    dense_ms = d0.elapsed_time(d1) / dense_steps
+    dense_ms = statistics.median(timed_regions(torch, stream, g_dense.replay, 3,
+                                               lambda: None)) / dense_steps
     dense_bytes = n * m_rows * d * 2 + n * 4
 
-    # end to end through the C ABI with host buffers: per step a pinned
-    # host -> device copy of x, the decode call, a device -> host copy of y
-    e2e_steps = min(args.steps, args.e2e_steps)
+    # end to end through the C ABI with host buffers, per token: a pinned
+    # host -> device copy of the token's x, one decode launch, a device ->
+    # host copy of its y (the line's e2e); and the same amortised over the
+    # G tokens of one launch (e2e_chunked)
     xh = torch.from_numpy(np.concatenate(
         [synth.gen_x(w["seed"] + 7 + 1000 * rank, s, 1, d) for s in range(G)])).pin_memory()
     yh = torch.empty((G, d), dtype=torch.float32).pin_memory()
-    xin = torch.empty((1, d), dtype=torch.float32, device=dev)
+    xin = torch.empty((G, d), dtype=torch.float32, device=dev)
+    e2e_tokens = min(K, 200)
 
-    if seq:
-        xin_all = torch.empty((G, d), dtype=torch.float32, device=dev)
+    def e2e_tok():
+        for s in range(e2e_tokens):
+            xin[s % G].copy_(xh[s % G], non_blocking=True)
+            launch(1, xin[s % G], ys[s % G], None)
+            yh[s % G].copy_(ys[s % G], non_blocking=True)
 
-    def estep(s):
-        if seq:  # one call: the chunk's G inputs up, G decode steps, G outputs down
-            xin_all.copy_(xh, non_blocking=True)
-            step(s, cnt_slot=False, xsrc=xin_all)
+    def e2e_chunk():
+        for _ in range(launches_per_region):
+            xin.copy_(xh, non_blocking=True)
+            launch(G, xin, ys, None)
             yh.copy_(ys, non_blocking=True)
-            return
-        xin.copy_(xh[s % G:s % G + 1], non_blocking=True)
-        step(s, cnt_slot=False, xsrc=xin)
-        yh[s % G:s % G + 1].copy_(y, non_blocking=True)
 
     with torch.cuda.stream(stream):
-        for s in range(1 if seq else 2):
-            estep(s)
-    stream.synchronize()
-    g_e2e = capture(calls_per_graph, estep)
+        e2e_tok()
+        e2e_chunk()
+        stream.synchronize()
+    g_e2e = capture(e2e_tok)
+    g_e2c = capture(e2e_chunk)
     with torch.cuda.stream(stream):
         g_e2e.replay()
-        stream.synchronize()
-        f0 = torch.cuda.Event(enable_timing=True)
-        f1 = torch.cuda.Event(enable_timing=True)
-        f0.record(stream)
-        full = max(1, e2e_steps // G)
-        for _ in range(full):
-            g_e2e.replay()
-        f1.record(stream)
-    stream.synchronize()
-    e2e_ms = f0.elapsed_time(f1)
-    e2e_done = full * G
-    e2e_value, _ = aggregate([max_over_ranks(e2e_ms, world, dev)], [e2e_done * world], world)
+        g_e2c.replay()
+    e2e_ms = statistics.median(timed_regions(torch, stream, g_e2e.replay, args.repeats, barrier))
+    e2c_ms = statistics.median(timed_regions(torch, stream, g_e2c.replay, args.repeats, barrier))
+    e2e_value, _ = aggregate([max_over_ranks(e2e_ms, world, dev)], [e2e_tokens * world], world)
+    e2c_value, _ = aggregate([max_over_ranks(e2c_ms, world, dev)], [K * world], world)
 
     if rank != 0:
         if world > 1:
@@ -450,41 +553,39 @@ def run_ours(args):
                "sample": f"first {done} decode steps of {args.workload} (time-bounded at "
                          f"{budget:.0f} s), fp64 oracle predict+compact+sparse FFN"}
 
-    kernel_key = (f"seq_kernel:{args.workload}" if seq else f"ffn_kernel_fused:{args.workload}")
+    config = layer_config(w, args, hot, R, layer_bytes, step_bytes_est, l2)
+    config["steps_per_launch"] = G
+    config["parallelism"] = "replicas" if world > 1 else "single GPU"
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic",
-        "config": {
-            "workload": args.workload, "batch": 1, "weights": w["dtype"], "density": w["density"],
-            "d": d, "n": n, "r": r, "gated": gated, "hot_prefix": hot, "layout": args.layout,
-            "l2": (f"inputs larger than L2: {R} rotating weight replicas "
-                   f"({R * layer_bytes / 1e9:.1f} GB; each step reads its own copy)"
-                   if R * step_bytes_est >= 3 * l2 else
-                   f"L2-warm (not HBM-bound): {R} weight replica(s) of "
-                   f"{layer_bytes / 1e9:.2f} GB reused across steps"),
-            "graph_len": G, "parallelism": "replicas" if world > 1 else "single GPU",
-        },
+        "data": "synthetic", "config": config,
+        "repeats": args.repeats, "regions_ms": regions,
         "us_per_layer": ms_per_step * 1e3,
         "active_neurons_mean": mean_cnt,
         "bytes_per_step": {"predictor": pred_bytes, "active_rows": active_bytes,
                            "total": alg_bytes},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": stored_traffic(kernel_key),
+                     "frac": achieved / peak, "traffic": traffic,
                      "peak_kind": f"{peak_kind} copy bandwidth",
-                     "kernel": (f"seq_kernel (persistent, {G} decode steps per launch)" if seq
-                                else "ffn_kernel (fused predictor+compaction+FFN, one launch/step)")},
+                     "kernel": f"seq_kernel (persistent, {G} decode steps per launch)",
+                     "traffic_how": ("ncu dram__bytes_read.sum + dram__bytes_write.sum per step "
+                                     f"(profiles/traffic.json) x {G} steps per launch"
+                                     if tr else "null: no capture of the current kernel source")},
         "dense_ffn": {"us_per_step": dense_ms * 1e3, "tokens_per_s": 1e3 / dense_ms,
                       "achieved_gbs": dense_bytes / (dense_ms / 1e3) / 1e9,
                       "frac": dense_bytes / (dense_ms / 1e3) / 1e9 / peak},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": d * 4,
-                "d2h_bytes_per_step": d * 4, "steps": e2e_done,
-                "how": (f"CUDA-graph replay per {G} steps of (pinned H2D of their x, one "
-                        f"pi_decode_layers launch, D2H of their y)" if seq else
-                        "CUDA-graph replay of (pinned H2D x, pi_layer_decode, D2H y) per step")},
-        "gpu_launches": launches,
-        "engine": args.engine,
+                "d2h_bytes_per_step": d * 4, "steps": e2e_tokens,
+                "how": "per token: pinned H2D of its x, one pi_decode_layers launch (one step), "
+                       "D2H of its y; CUDA-graph replay"},
+        "e2e_chunked": {"value": e2c_value, "unit": "tokens/s", "h2d_bytes_per_step": d * 4,
+                        "d2h_bytes_per_step": d * 4, "steps": K,
+                        "how": f"per launch of {G} tokens: one pinned H2D of their x, one "
+                               f"pi_decode_layers launch, one D2H of their y"},
+        "gpu_launches": launches_per_region,
+        "engine": "seq",
         "clocks": clocks,
         "cpu_baseline": cpu,
         "csrc_hash": csrc_hash(),
@@ -497,14 +598,12 @@ def run_ours(args):
     return 0
 
 
+# ------------------------------------------------------------------ our arm: the stack
 def run_stack(args):
-    """One step = one token through every layer of a residual FFN stack
-    (x_{l+1} = x_l + FFN_l(x_l)): one pi_decode_layers launch per token
-    through all layers (engine seq, the default), or pi_layer_decode per
-    layer (engine call).  The layers are
-    generated on the GPU (the stack is too large for the host generator to
-    make quickly) and packed; the weights of all layers together exceed L2
-    many times over, so every layer's weights come from HBM."""
+    """One step = one token through every layer of the residual FFN stack
+    (x_{l+1} = x_l + FFN_l(x_l)): one pi_decode_layers launch per token.
+    The weights of all layers together exceed L2 hundreds of times over, so
+    every layer's weights come from HBM."""
     import torch
 
     import activation_sparse_decode_rank_gb300 as pi
@@ -518,98 +617,155 @@ def run_stack(args):
     torch.cuda.set_device(dev)
     pi.build()
     w = workload_spec(args.workload)
-    d, n, r, L = w["d"], w["n"], w["r"], w["layers"]
-    alpha, rho, cz, scale = synth.stack_plan(w["seed"], L, n)
-    descs, wts, keep, pred_bytes = [], [], [], 0
-    for l in range(L):
-        g = synth.make_layer_gpu(d, n, r, w["dtype"], alpha=float(alpha[l]), zipf_c=float(cz[l]),
-                                 seed=w["seed"], layer=l, bias_scale=float(scale[l]), device=dev)
-        p = synth.zipf_probs(n, float(alpha[l]), float(cz[l]))
-        hot = int((p >= 0.5).sum()) if args.hot < 0 else args.hot
-        desc = pi.make_desc(d, n, r, w["dtype"], False, hot, packed=True)
-        rec = torch.empty((n, 2 * d), dtype=torch.int16, device=dev)
-        pi.check(pi.pi_pack_weights(desc, g["W1"], g["W2"], rec), "pi_pack_weights")
-        torch.cuda.synchronize()
-        del g["W1"], g["W2"]
-        keep.append((g, rec))
-        descs.append(desc)
-        wts.append(pi.make_weights(g["A"], g["Bm"], g["b1"], rec, None, g["b2"]))
-        pred_bytes += n * r * 2 + r * d * 2 + n * 4
-    torch.cuda.empty_cache()
-    G = min(args.steps, args.graph_len)
+    w["name"] = args.workload
+    d, n, r = w["d"], w["n"], w["r"]
+    L = args.layers if args.layers > 0 else w["layers"]
+    descs, wts, keep, pred_bytes = build_stack(w, dev, L)
+    K = args.steps
     xs = torch.from_numpy(np.concatenate(
-        [synth.gen_x(w["seed"] + 1000 * rank, s, 1, d) for s in range(G)])).to(dev)
-    xbuf = torch.empty((L + 1, d), dtype=torch.float32, device=dev)
-    cnts = torch.zeros((G, L, 4), dtype=torch.int32, device=dev)
-    cseq = torch.zeros((G, (L + 3) // 4 * 4), dtype=torch.int32, device=dev)  # 16-byte rows
+        [synth.gen_x(w["seed"] + 1000 * rank, s, 1, d) for s in range(K)])).to(dev)
+    ybuf = torch.empty((K, L, d), dtype=torch.float32, device=dev)
+    cseq = torch.zeros((K, (L + 3) // 4 * 4), dtype=torch.int32, device=dev)  # 16-byte rows
     st = torch.zeros(4, dtype=torch.int32, device=dev)
     ws = pi.workspace(descs[0], 1, dev)
     stream = torch.cuda.Stream(device=dev)
 
-    seq = args.engine == "seq"
+    def token(s, xsrc, cnt=True):
+        # the whole stack for one token in one persistent launch; y[l] = x_{l+1}
+        pi.check(pi.pi_decode_layers(descs, wts, L, xsrc, 1, ybuf[s], cseq[s] if cnt else None,
+                                     None, st, ws, stream=stream), "pi_decode_layers")
 
-    def step(s):
-        if seq:  # the whole stack for one token in one persistent launch
-            pi.check(pi.pi_decode_layers(descs, wts, L, xs[s % G], 1, xbuf[1:], cseq[s % G],
-                                         None, st, ws, stream=stream), "pi_decode_layers")
-            return
-        for l in range(L):
-            xin = xs[s % G] if l == 0 else xbuf[l]
-            pi.check(pi.pi_layer_decode(descs[l], wts[l], xin, 1, xbuf[l + 1], xin, None,
-                                        cnts[s % G, l], st, ws, stream=stream), "pi_layer_decode")
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+        return g
 
     with torch.cuda.stream(stream):
-        step(0)
+        token(0, xs[0])
         stream.synchronize()
-    g_main = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        with torch.cuda.graph(g_main, stream=stream):
-            for s in range(G):
-                step(s)
-    reps = max(1, args.steps // G)
-    with torch.cuda.stream(stream):
-        for _ in range(max(1, math.ceil(args.warmup / G))):
+    if int(st[0]) != 0:
+        raise SystemExit(f"bench: device status {pi.status_string(int(st[0]))}")
+    g_main = capture(lambda: [token(s, xs[s]) for s in range(K)])
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    with torch.cuda.stream(stream):  # warm-up (untimed): at least W tokens
+        for _ in range(max(1, math.ceil(args.warmup / K))):
             g_main.replay()
         stream.synchronize()
     sampler = ClockSampler(local)
     sampler.start()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(reps):
-            g_main.replay()
-        e1.record(stream)
-    stream.synchronize()
+    regions = timed_regions(torch, stream, g_main.replay, args.repeats, barrier)
     clocks = sampler.stop()
-    ms = e0.elapsed_time(e1)
-    steps = reps * G
     if int(st[0]) != 0:
         raise SystemExit(f"bench: device status {pi.status_string(int(st[0]))}")
-    mean_cnt = (cseq[:, :L] if seq else cnts[:, :, 0]).float().mean(dim=0).cpu().numpy()
+    ms = statistics.median(regions)
+    mean_cnt = cseq[:, :L].float().mean(dim=0).cpu().numpy()
     alg_bytes = pred_bytes + float(mean_cnt.sum()) * 2 * d * 2
-    ms_step = ms / steps
+    value, t_max = aggregate([max_over_ranks(ms, world, dev)], [K * world], world)
+    ms_step = t_max / K
     peak, peak_kind = measured_peaks()
-    achieved = alg_bytes / (ms_step / 1e3) / 1e9
+    achieved = alg_bytes / (ms / K / 1e3) / 1e9
+    tr = stored_traffic(f"seq_kernel:{args.workload}:{L}")
+    traffic = tr[0] if tr else None  # one launch = one step (one token)
+
+    # dense comparison point: pi_dense_ffn over every layer of the stack
+    ws_d = pi.workspace(descs[0], 1, dev)
+    yd = torch.empty((1, d), dtype=torch.float32, device=dev)
+
+    def dense_token():
+        for l in range(L):
+            pi.check(pi.pi_dense_ffn(descs[l], wts[l], xs[0], 1, yd, ws_d, stream=stream))
+
+    with torch.cuda.stream(stream):
+        dense_token()
+    g_dense = capture(dense_token)
+    with torch.cuda.stream(stream):
+        g_dense.replay()
+    dense_ms = statistics.median(timed_regions(torch, stream, g_dense.replay, 3, lambda: None))
+    dense_bytes = L * (n * 2 * d * 2 + n * 4)
+
+    # end to end through the C ABI with host buffers, per token: a pinned
+    # H2D copy of the token's x, one pi_decode_layers launch through all
+    # layers, a D2H copy of its output x_L
+    xh = torch.from_numpy(np.concatenate(
+        [synth.gen_x(w["seed"] + 7 + 1000 * rank, s, 1, d) for s in range(K)])).pin_memory()
+    yh = torch.empty((K, d), dtype=torch.float32).pin_memory()
+    xin = torch.empty((K, d), dtype=torch.float32, device=dev)
+
+    def e2e():
+        for s in range(K):
+            xin[s].copy_(xh[s], non_blocking=True)
+            token(s, xin[s], cnt=False)
+            yh[s].copy_(ybuf[s, L - 1], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e()
+        stream.synchronize()
+    g_e2e = capture(e2e)
+    with torch.cuda.stream(stream):
+        g_e2e.replay()
+    e2e_ms = statistics.median(timed_regions(torch, stream, g_e2e.replay, args.repeats, barrier))
+    e2e_value, _ = aggregate([max_over_ranks(e2e_ms, world, dev)], [K * world], world)
+    if int(st[0]) != 0:
+        raise SystemExit(f"bench: device status {pi.status_string(int(st[0]))}")
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        budget = float(os.environ.get("PI_CPU_BUDGET_S", "15"))
+        done, dt, cores = stack_oracle_sample(w, keep, 16, 1, budget, seed_off=13)
+        cpu = {"value": done / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{done} tokens (after 1 untimed) through all {L} layers, fp64 oracle "
+                         f"predict+compact+sparse FFN + residual per layer (layers visited one at "
+                         f"a time; time-bounded at {budget:.0f} s)"}
+
+    config = stack_config(w, L)
+    config["parallelism"] = "replicas" if world > 1 else "single GPU"
     line = {
-        "metric": METRIC, "value": steps / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1,
-        "steps": steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": args.workload, "batch": 1, "layers": L, "weights": w["dtype"],
-                   "d": d, "n": n, "r": r, "layout": "packed",
-                   "l2": f"inputs larger than L2: {L} distinct layers resident "
-                         f"({L * (n * 2 * d * 2 + n * r * 2 + r * d * 2) / 1e9:.1f} GB)"},
+        "config": config,
+        "repeats": args.repeats, "regions_ms": regions,
         "us_per_token": ms_step * 1e3, "us_per_layer": ms_step * 1e3 / L,
         "density_per_layer": [float(v) / n for v in mean_cnt],
         "bytes_per_step": {"predictor": pred_bytes, "active_rows": alg_bytes - pred_bytes,
                            "total": alg_bytes},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
-                     "peak_kind": f"{peak_kind} copy bandwidth"},
-        "gpu_launches": steps * (1 if seq else L), "engine": args.engine,
-        "clocks": clocks, "csrc_hash": csrc_hash(),
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_kind": f"{peak_kind} copy bandwidth",
+                     "kernel": f"seq_kernel (persistent, one token through {L} layers per launch)",
+                     "traffic_how": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one "
+                                     "launch (profiles/traffic.json)" if tr else
+                                     "null: no capture of the current kernel source")},
+        "dense_ffn": {"us_per_token": dense_ms * 1e3 / L * L, "us_per_layer": dense_ms * 1e3 / L,
+                      "tokens_per_s": 1e3 / dense_ms,
+                      "achieved_gbs": dense_bytes / (dense_ms / 1e3) / 1e9,
+                      "frac": dense_bytes / (dense_ms / 1e3) / 1e9 / peak},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": d * 4,
+                "d2h_bytes_per_step": d * 4, "steps": K,
+                "how": "per token: pinned H2D of its x, one pi_decode_layers launch through all "
+                       "layers, D2H of its output; CUDA-graph replay"},
+        "gpu_launches": K, "engine": "seq",
+        "clocks": clocks, "cpu_baseline": cpu, "csrc_hash": csrc_hash(),
     }
     print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
     return 0
 
 
@@ -854,37 +1010,43 @@ def run_reorder(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200000)
-    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="decode steps per timed region (default: 100 for the stack, 20000 "
+                         "for one layer)")
+    ap.add_argument("--warmup", type=int, default=None, help="untimed steps first (>= 3)")
+    ap.add_argument("--repeats", type=int, default=5,
+                    help="timed regions of --steps steps each; the median is reported")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="stack only: decode through its first LAYERS layers (0: all)")
     ap.add_argument("--replicas", type=int, default=0)
     ap.add_argument("--layout", default="packed", choices=["packed", "split"])
     ap.add_argument("--hot", type=int, default=-1, help="hot-prefix length (-1: p_i >= 0.5)")
-    ap.add_argument("--graph-len", type=int, default=2000)
-    ap.add_argument("--e2e-steps", type=int, default=20000)
+    ap.add_argument("--graph-len", type=int, default=2000,
+                    help="one layer: decode steps per pi_decode_layers launch")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--engine", default="auto", choices=["auto", "call", "seq"],
-                    help="call: one pi_layer_decode launch per step (per layer); seq: "
-                         "pi_decode_layers, one persistent launch per graph-length chunk of "
-                         "steps (per token for a stack); auto: seq (faster on one layer, "
-                         "the same on the 48-layer stack, as measured on GB300)")
     ap.add_argument("--reorder", action="store_true",
                     help="offline profiling + neuron placement timings for --workload")
     ap.add_argument("--sweep", action="store_true",
                     help="batched decode / density sweep (with --workload opt13b_ffn_batched_...)")
     args = ap.parse_args()
+    from synth.workloads import WORKLOADS
+    stack = WORKLOADS[args.workload].get("layers", 1) > 1
+    if args.steps is None:
+        args.steps = 100 if stack else 20000
+    if args.warmup is None:
+        args.warmup = 5 if stack else 2000
     if args.warmup < 3:
         raise SystemExit("bench: at least 3 warm-up steps")
+    if args.repeats < 1:
+        raise SystemExit("bench: at least one timed region")
     if args.impl == "reference":
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
     if args.reorder:
         return run_reorder(args)
-    stack = workload_spec(args.workload).get("layers", 1) > 1
-    if args.engine == "auto":
-        args.engine = "seq"
     if stack:
         return run_stack(args)
     return run_ours(args)

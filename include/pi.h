@@ -76,8 +76,10 @@ typedef enum {
   PI_ERR_TIMEOUT = 8,    /* device: a bounded grid-wide wait ran out           */
   PI_ERR_CUDA = 9,       /* a CUDA runtime call failed                         */
   PI_ERR_INDEX = 10,     /* device: an active-list entry is outside [0, n)     */
-  PI_ERR_RANGE = 11      /* device: a predictor partial sum exceeds the range
+  PI_ERR_RANGE = 11,     /* device: a predictor partial sum exceeds the range
                             of the fixed-point exchange (|value| >= 2^23)      */
+  PI_ERR_CAPTURE = 12    /* a call's one-time setup was asked for while its
+                            stream was being captured into a CUDA graph        */
 } pi_status;
 
 typedef enum { PI_F16 = 0, PI_BF16 = 1 } pi_dtype;
@@ -179,7 +181,9 @@ pi_status pi_sparse_ffn(const pi_ffn_desc* desc, const pi_layer_weights* w,
                         int32_t* dev_status, void* ws, size_t ws_bytes,
                         pi_stream stream);
 
-/* Dense FFN over all n neurons, the comparison point of the sparse path:
+/* Dense FFN over all n neurons, the comparison point of the sparse path.
+ * The paper has no counterpart passage: this call is the baseline that the
+ * sparse calls are measured against (every row read, no predictor):
  *     y[t] = b2 + sum_i ReLU(W1_i . x[t] + b1_i) W2_i   (gated as above).
  * batch <= 32.  batch > 1 with d % 128 == 0 reads every row once for all
  * tokens on the tensor cores (the batched sparse path over all n neurons);
@@ -241,16 +245,19 @@ pi_status pi_decode_layers(const pi_ffn_desc* descs, const pi_layer_weights* lay
  * Inputs and outputs are the caller's, as in pi_layer_decode with batch = 1
  * and ws = NULL.  The scratch is a fixed array of PI_STATIC_SCRATCH_BYTES in
  * the library's device image, held by every GPU that loads the library until
- * the process exits.  Shapes whose scratch does not fit (about P * d * 4
- * bytes of partial sums plus n bytes, P = the GPU's SM count) are rejected
- * with PI_ERR_WORKSPACE before anything is launched.  The call allocates and
- * frees nothing; each call clears the array's barrier block with one
- * cudaMemsetAsync on `stream` before its launch.  The first call on a device
- * looks up the array's device address (cudaGetSymbolAddress, with that
- * device current); make that first call before any stream capture.  All
- * calls share the one array: calls that overlap on the GPU (other streams,
- * other threads) race and corrupt each other's results; issue them in one
- * stream order. */
+ * the process exits.  A shape needs
+ *     ru(256) + ru(32 r) + ru(4 P) + ru(n) + ru(4 P d)   bytes,
+ * ru() rounding up to a multiple of 256 and P the GPU's SM count (at most
+ * 512); shapes that need more are rejected with PI_ERR_WORKSPACE before
+ * anything is launched (before any CUDA call when even P = 1 would not fit).
+ * The call allocates and frees nothing; each call clears the array's barrier
+ * block with one cudaMemsetAsync on `stream` before its launch.  The first
+ * call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture: made while `stream` is being captured it
+ * returns PI_ERR_CAPTURE and launches nothing.  All calls share the one
+ * array: calls that overlap on the GPU (other streams, other threads) race
+ * and corrupt each other's results; issue them in one stream order. */
 #define PI_STATIC_SCRATCH_BYTES (8u << 20)
 pi_status pi_layer_decode_static(const pi_ffn_desc* desc, const pi_layer_weights* w,
                                  const float* x, float* y, const float* residual,
@@ -361,6 +368,82 @@ pi_status pi_plan_dispatch(const pi_ffn_desc* desc, int32_t batch, const float* 
                            float density, int32_t allow_dense, const pi_cost_model* model,
                            pi_plan* out);
 
+/* Runs one decode step through `path` (a pi_path, e.g. pi_plan.path):
+ *   PI_PATH_FUSED      batch == 1: pi_layer_decode;
+ *   PI_PATH_PER_TOKEN  one batch-1 pi_layer_decode per token;
+ *   PI_PATH_UNION      batch 2..32, d % 128 == 0: pi_layer_decode's union
+ *                      path (the tokens' active rows read once, tensor cores);
+ *   PI_PATH_DENSE      pi_dense_ffn (+ residual): the plain dense FFN, not
+ *                      the predicted-sparse result; idx_out / cnt_out are not
+ *                      written.
+ * Arguments as in pi_layer_decode (ws of pi_workspace_size(desc, batch)
+ * bytes or more).  The first three paths give the same result: each token
+ * uses its own predicted set ("PowerInfer: Quick Massive Language Mannequin
+ * Serving with a Client-grade GPU", "Online Section").  PI_ERR_SHAPE for a
+ * path the batch or shape does not allow. */
+pi_status pi_decode_planned(const pi_ffn_desc* desc, const pi_layer_weights* w, int32_t path,
+                            const float* x, int32_t batch, float* y, const float* residual,
+                            int32_t* idx_out, int32_t* cnt_out, int32_t* dev_status, void* ws,
+                            size_t ws_bytes, pi_stream stream);
+
+/* A decoder: one layer, its activation profile and fixed buffers, executing
+ * the dispatch plan with one captured CUDA graph per batch size (the tiers of
+ * "Efficient, VRAM-Constrained xLM Inference on Clients", "Methodology, A.
+ * Pipelined Sharding": a plan per number of tokens per step, chosen by the
+ * time estimator).
+ *   pi_decoder_create: desc / w as in pi_layer_decode; p_active, density,
+ *     allow_dense, model as in pi_plan_dispatch (p_active is copied); x
+ *     [32][d] and y [32][d] fp32, residual NULL or [32][d], dev_status and ws
+ *     (pi_workspace_size(desc, 32) bytes, zero-filled) are device buffers
+ *     the decoder reads and writes on every run; they must outlive it.
+ *     Creates a non-blocking stream for its captures (current device).
+ *   pi_decoder_run: decodes tokens x[0 .. batch) into y[0 .. batch) through
+ *     the path planned for this batch.  The first run of a batch size runs
+ *     the calls directly on `stream`, then captures them into a graph; later
+ *     runs of that size launch the graph on `stream`.  If `stream` is being
+ *     captured by the caller, the calls are recorded into the caller's graph
+ *     and no graph of the decoder's is made.  Runs of one decoder must not
+ *     overlap on the GPU (they share ws).  PI_ERR_SHAPE on another device.
+ *   pi_decoder_plan: the plan used for a batch size.
+ *   pi_decoder_destroy: releases the graphs and the stream (after the
+ *     caller's last run has completed). */
+typedef struct pi_decoder pi_decoder;
+pi_status pi_decoder_create(const pi_ffn_desc* desc, const pi_layer_weights* w,
+                            const float* p_active, float density, int32_t allow_dense,
+                            const pi_cost_model* model, const float* x, float* y,
+                            const float* residual, int32_t* dev_status, void* ws, size_t ws_bytes,
+                            pi_decoder** out);
+pi_status pi_decoder_run(pi_decoder* dec, int32_t batch, pi_stream stream);
+pi_status pi_decoder_plan(pi_decoder* dec, int32_t batch, pi_plan* out);
+void pi_decoder_destroy(pi_decoder* dec);
+
+/* Neuron-sharded decode across G ranks (one GPU each).  Neurons are
+ * independent until the down projection adds their column vectors ("PowerInfer:
+ * Quick Massive Language Mannequin Serving with a Client-grade GPU", "Neuron
+ * Conscious Operator"), so rank g of G can hold the neurons i = g, g + G,
+ * g + 2G, ... of the hot-first order (its neuron table: local row k is
+ * neuron g + k G, "Neuron Placement and Administration") with a full copy
+ * of Bm, and decode them with the ordinary calls into a partial output
+ * (b2 on one rank only, no residual).  One exchange of the G partial
+ * outputs (d floats per token, e.g. an all-gather over the ranks) and
+ * pi_shard_reduce complete the layer.
+ *   pi_shard_desc: the shard's descriptor (host only): n = the rank's neuron
+ *     count, hot_prefix = its neurons below the layer's hot prefix (still a
+ *     prefix of its rows); G in 1..1024, 0 <= g < min(G, n).
+ *   pi_shard_layer: copies rows g, g + G, ... of A, b1, W1 (gated: gate|up;
+ *     packed: whole records) and W2 (split layout) into dst, whose buffers
+ *     hold the shard's rows (sizes from pi_shard_desc) and differ from src's;
+ *     dst->Bm and dst->b2 are not written (pass src->Bm, and b2 on one rank).
+ *     Asynchronous strided device-to-device copies on `stream`.
+ *   pi_shard_reduce: y[t] = residual[t] (or 0) + sum over g = 0, 1, ..., G-1
+ *     of parts[g][t], in that order (deterministic); parts [G][batch][d],
+ *     residual NULL or [batch][d], y [batch][d] fp32; batch <= 32. */
+pi_status pi_shard_desc(const pi_ffn_desc* desc, int32_t G, int32_t g, pi_ffn_desc* out);
+pi_status pi_shard_layer(const pi_ffn_desc* desc, const pi_layer_weights* src, int32_t G,
+                         int32_t g, const pi_layer_weights* dst, pi_stream stream);
+pi_status pi_shard_reduce(const float* parts, int32_t G, int32_t batch, int32_t d,
+                          const float* residual, float* y, pi_stream stream);
+
 /* Static text of a status code. */
 const char* pi_status_string(pi_status s);
 
@@ -370,6 +453,18 @@ const char* pi_status_string(pi_status s);
  * zero-filled workspace of pi_workspace_size(desc, 1) bytes for some valid
  * desc; it must be zero-filled again afterwards.  Returns PI_OK when the
  * launch was issued. */
+/* Diagnostic of the ring's failure path: pi_sparse_ffn for batch 1, except
+ * that in every block the copy of the first listed neuron's rows is never
+ * issued, so the compute warps' wait for it runs out after limit_ns
+ * nanoseconds (1e3 .. 5e9).  The block then abandons its ring, lets every
+ * copy it did issue land, and PI_ERR_TIMEOUT lands in *dev_status; y is not
+ * meaningful.  Arguments as in pi_sparse_ffn (batch 1); ws must be zero-filled
+ * again afterwards.  Returns PI_OK when the launch was issued. */
+pi_status pi_selftest_ring_timeout(const pi_ffn_desc* desc, const pi_layer_weights* w,
+                                   const float* x, const int32_t* idx, const int32_t* cnt,
+                                   int32_t cap, float* y, int32_t* dev_status, void* ws,
+                                   size_t ws_bytes, int64_t limit_ns, pi_stream stream);
+
 pi_status pi_selftest_wait_timeout(int32_t* dev_status, void* ws,
                                    size_t ws_bytes, int64_t limit_ns,
                                    pi_stream stream);

@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for s in range(12):
+    for s in range(13):
         assert len(pi.status_string(s)) >= 2
     assert pi.status_string(0) == "ok"
     assert "unknown" in pi.status_string(99)
@@ -175,3 +175,16 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(pi, "_lib", None)
     with pytest.raises(RuntimeError, match="libpi.so not found"):
         pi.lib()
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="addresses below are stand-ins: run only where no GPU is visible")
+def test_static_scratch_rejects_shapes_beyond_its_size(lib):
+    # n bytes of mask alone fill the fixed scratch: refused before any CUDA
+    # call (no GPU exists here, so a CUDA call would have failed instead)
+    n = pi.PI_STATIC_SCRATCH_BYTES
+    desc = pi.make_desc(8192, n, 64, "f16")
+    fake = 1 << 40  # never dereferenced: the call returns before launching
+    w = pi.make_weights(fake, fake, fake, fake, fake, None)
+    rc = pi.pi_layer_decode_static(desc, w, fake, fake, None, None, None, fake, stream=0)
+    assert rc == pi.PI_ERR_WORKSPACE

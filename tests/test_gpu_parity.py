@@ -406,3 +406,37 @@ def test_bounded_wait_times_out_and_reports():
     x = synth.gen_x(35, 0, 1, D.L.d)
     o = _decode(D, x)
     assert o["status"] == 0
+
+
+@pytest.mark.parametrize("packed", [False, True])
+def test_ring_wait_times_out_and_returns(packed):
+    # every block's first listed neuron is never copied: its ring wait runs
+    # out after 2 ms, the block abandons its ring (issuing nothing more and
+    # letting what it issued land) and the launch ends within about one bound
+    import time
+    D = layer("tiny_d1024_n4096")
+    D.set_packed(packed)
+    L = D.L
+    n = L.n
+    idx = torch.arange(n, dtype=torch.int32, device=DEV)  # 26+ neurons per block
+    cnt = torch.tensor([n, 0, 0, 0], dtype=torch.int32, device=DEV)
+    x = up(synth.gen_x(36, 0, 1, L.d), DEV)
+    y = torch.empty((1, L.d), device=DEV)
+    ws = D.workspace()
+    st = zeros_i32(1, DEV)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    pi.check(pi.pi_selftest_ring_timeout(D.desc, D.w, x, idx, cnt, n, y, st, ws, 2_000_000))
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert int(st[0]) == pi.PI_ERR_TIMEOUT
+    assert dt < 0.5, f"a timed-out ring took {dt:.3f} s to return"
+    # the context is still usable: the same list decodes normally
+    ws2 = D.workspace()
+    st2 = zeros_i32(1, DEV)
+    pi.check(pi.pi_sparse_ffn(D.desc, D.w, x, 1, idx, cnt, n, None, None, None, y, st2, ws2))
+    torch.cuda.synchronize()
+    assert int(st2[0]) == 0
+    xh = synth.gen_x(36, 0, 1, L.d)[0]
+    assert y_rel_err(L, xh, np.arange(n, dtype=np.int32), y[0].cpu().numpy()) <= Y_TOL
+    D.set_packed(False)

@@ -11,6 +11,7 @@ import socket
 import subprocess
 import sys
 
+import numpy as np
 import pytest
 import torch.multiprocessing as mp
 
@@ -62,14 +63,45 @@ def test_max_over_ranks_single_rank_is_identity():
 def test_reference_arm_prints_on_rank_zero_only(tmp_path):
     env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1", PI_REF_BUDGET_S="1")
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
-                        "--steps", "2", "--warmup", "3", "--gpus", "2"],
+                        "--steps", "2", "--warmup", "3", "--gpus", "2",
+                        "--workload", "opt6.7b_ffn_d4096_n16384_r128_f16"],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0 and r.stdout.strip() == ""
     env.update(RANK="0", LOCAL_RANK="0")
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
-                        "--steps", "2", "--warmup", "3", "--gpus", "2"],
+                        "--steps", "2", "--warmup", "3", "--gpus", "2",
+                        "--workload", "opt6.7b_ffn_d4096_n16384_r128_f16"],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_stack_oracle_sample_walks_every_layer_on_the_host():
+    # the CPU baseline of the layer stack, on a tiny 3-layer stack built by
+    # the host generator: every token goes through every layer in order
+    import torch
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    import synth
+    w = dict(d=64, n=256, r=16, dtype="f16", seed=9, layers=3)
+    keep, hosts = [], []
+    for l in range(3):
+        L = synth.make_layer(64, 256, 16, "f16", alpha=0.9, density=0.1, seed=9, layer=l)
+        rec = np.concatenate([L.W1, L.W2], axis=1).view(np.int16)
+        g = {"A": torch.from_numpy(L.A.view(np.int16)), "Bm": torch.from_numpy(L.Bm.view(np.int16)),
+             "b1": torch.from_numpy(L.b1), "b2": torch.from_numpy(L.b2)}
+        keep.append((g, torch.from_numpy(rec)))
+        hosts.append(L)
+    done, dt, cores = bench.stack_oracle_sample(w, keep, tokens=4, warm=1, budget_s=60.0)
+    assert done == 4 and dt > 0 and cores >= 1
+    # the host copy of a packed layer is the layer itself
+    H = bench.host_layer(w, keep[1][0], keep[1][1])
+    for a, b in [(H.A, hosts[1].A), (H.Bm, hosts[1].Bm), (H.W1, hosts[1].W1),
+                 (H.W2, hosts[1].W2), (H.b1, hosts[1].b1)]:
+        np.testing.assert_array_equal(a, b)
+    x = synth.gen_x(9, 0, 1, 64)[0]
+    assert np.array_equal(oracle.layer_decode(H, x, residual=True)[3],
+                          oracle.layer_decode(hosts[1], x, residual=True)[3])

@@ -12,9 +12,8 @@ import pytest
 import torch
 
 import activation_sparse_decode_rank_gb300 as pi
-import oracle
 import synth
-from pihelp import DevLayer, Y_TOL, up, zeros_i32
+from pihelp import DevLayer, Y_TOL, up, y_rel_err, zeros_i32
 
 pytestmark = pytest.mark.gpu
 
@@ -56,18 +55,23 @@ def test_static_scratch_matches_workspace_call(shape):
         y0, i0, s0 = _run(D, x, static=False)
         y1, i1, s1 = _run(D, x, static=True)
         assert s0 == 0 and s1 == 0
+        # the same kernel, grid and summation order on both calls: identical
+        # bits (a stale or aliased region of the shared array would show here)
         np.testing.assert_array_equal(i1, i0)
-        yd = oracle.dense_ffn(L, x[0])
-        assert float(np.abs(y1 - y0).max()) <= Y_TOL * float(np.abs(yd).max())
+        np.testing.assert_array_equal(y1, y0)
+        # and the result itself within the oracle tolerance on the GPU's list
+        assert y_rel_err(L, x[0], i0, y0) <= Y_TOL
 
 
-def test_static_scratch_rejects_shapes_beyond_its_size():
-    # d = 8192 partial sums over every SM plus n mask bytes exceed the array
-    P = torch.cuda.get_device_properties(DEV).multi_processor_count
-    n = pi.PI_STATIC_SCRATCH_BYTES  # the mask alone fills it
-    desc = pi.make_desc(8192, n, 64, "f16")
-    w = pi.make_weights(1 << 40, 1 << 40, 1 << 40, 1 << 40, 1 << 40, None)
+def test_static_scratch_rejects_too_large_a_shape_on_the_gpu():
+    # the rejection happens on the host; every pointer is a real buffer of
+    # this test (small: the shape is refused before anything is launched)
+    d, n, r = 8192, pi.PI_STATIC_SCRATCH_BYTES, 64
+    desc = pi.make_desc(d, n, r, "f16")
+    buf = torch.zeros(4096, dtype=torch.float32, device=DEV)
+    w = pi.make_weights(buf, buf, buf, buf, buf, None)
     st = zeros_i32(1, DEV)
-    rc = pi.pi_layer_decode_static(desc, w, 1 << 40, 1 << 40, None, None, None, st)
+    rc = pi.pi_layer_decode_static(desc, w, buf, buf, None, None, None, st)
     assert rc == pi.PI_ERR_WORKSPACE
-    assert P > 0
+    torch.cuda.synchronize()
+    assert int(st[0]) == 0
