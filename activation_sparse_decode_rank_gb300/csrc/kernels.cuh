@@ -136,72 +136,92 @@ __device__ __forceinline__ void prefetch_neuron(const FfnArgs& a, int i) {
 }
 
 // ------------------------------------------------------------ predictor (fused)
-// Logits of this block's own neurons i = c + j P (j < rows), four lanes per
-// row, eight rows per warp at a time; flag[j] = (logit > 0).  A lane takes
-// the row's sixteen-byte pieces l, l + 4, ... in batches of four loads issued
-// before their first use (rows staged in shared memory, or read via L2).
+// Logits of this block's own neurons i = c + j P (j < rows); flag[j] =
+// (logit > 0).  A row's r/8 sixteen-byte pieces go to lpr lanes (the next
+// power of two), lane l holding piece l % lpr of u in registers for the whole
+// pass; a warp covers 32 / lpr rows per load, four loads in flight per lane;
+// each row's lpr partial dot products meet in a fixed xor tree.  Rows come
+// from shared memory (staged) or through L2.
 template <int DT>
-__device__ void own_logits(const FfnArgs& a, const unsigned char* As, const float* b1s,
-                           const float* us, unsigned char* flag, int rows) {
+__device__ __forceinline__ void own_logits(const FfnArgs& a, const unsigned char* As,
+                                           const float* b1s, const float* us,
+                                           unsigned char* flag, int rows) {
   const int rc = a.r >> 3;
+  const bool in_smem = a.a_in_smem != 0;
+  const int stride = a.a_stride, P = a.P, r = a.r;
+  const uint16_t* Ag = a.A;
   const int c = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, l = lane & 3;
-  constexpr int QT = 4;
-  for (int base = warp * 8; base < rows; base += kWarps * 8) {
-    const int j = base + g;
-    float acc = 0.f;
-    if (j < rows) {
-      for (int q0 = l; q0 < rc; q0 += 4 * QT) {
-        uint4 v[QT];
+  int lpr = 1;
+  while (lpr < rc) lpr <<= 1;  // <= 32 (r <= 256)
+  const int rpw = 32 / lpr;     // rows per warp and load
+  const int q = lane & (lpr - 1), sub = lane / lpr;
+  const bool qok = q < rc;
+  float u[8];
+  if (qok) {
+    load8(us + 8 * q, u);
+  } else {
 #pragma unroll
-        for (int t = 0; t < QT; ++t) {
-          const int q = q0 + 4 * t;
-          if (q < rc) {
-            if (a.a_in_smem)
-              v[t] = *reinterpret_cast<const uint4*>(As + (size_t)j * a.a_stride + 16 * q);
-            else
-              v[t] = ld_nc(a.A + ((size_t)c + (size_t)j * a.P) * a.r + 8 * q);
-          }
-        }
+    for (int e = 0; e < 8; ++e) u[e] = 0.f;
+  }
+  constexpr int RU = 4;          // rows per lane per pass
+  const int step = kWarps * rpw;  // rows between a lane's consecutive loads
+  for (int jb = warp * rpw; jb < rows; jb += step * RU) {  // warp-uniform bound
+    uint4 v[RU];
 #pragma unroll
-        for (int t = 0; t < QT; ++t) {
-          const int q = q0 + 4 * t;
-          if (q < rc) {
-            float f[8], u[8];
-            unpack8<DT>(v[t], f);
-            load8(us + 8 * q, u);
-            acc += dot8(f, u);
-          }
-        }
+    for (int t = 0; t < RU; ++t) {
+      const int jr = jb + sub + t * step;
+      v[t] = make_uint4(0u, 0u, 0u, 0u);
+      if (qok && jr < rows) {
+        if (in_smem)
+          v[t] = *reinterpret_cast<const uint4*>(As + (size_t)jr * stride + 16 * q);
+        else
+          v[t] = ld_nc(Ag + ((size_t)c + (size_t)jr * P) * r + 8 * q);
       }
     }
-    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-    if (j < rows && l == 0) flag[j] = (acc + b1s[j] > 0.f) ? 1 : 0;
+    float acc[RU];
+#pragma unroll
+    for (int t = 0; t < RU; ++t) {
+      float f[8];
+      unpack8<DT>(v[t], f);
+      acc[t] = dot8(f, u);
+    }
+    for (int o = lpr >> 1; o >= 1; o >>= 1)
+#pragma unroll
+      for (int t = 0; t < RU; ++t) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
+    if (q == 0) {
+#pragma unroll
+      for (int t = 0; t < RU; ++t) {
+        const int jr = jb + sub + t * step;
+        if (jr < rows) flag[jr] = (acc[t] + b1s[jr] > 0.f) ? 1 : 0;
+      }
+    }
   }
 }
 
 // ------------------------------------------------------------ FFN over a neuron list
-// Row-gather GEMV + ReLU and row-axpy over the m neurons of lst.  Rows reach
+// Row-gather GEMV + ReLU and row-axpy over the m neurons of lst (x: the
+// token's d activations, in shared or global memory).  Rows reach
 // shared memory by TMA bulk copies.  Entries [0, mh) are the block's own hot
 // neurons, armed up front into slots (lst[k] - c) / P; the other entries
 // cycle through slots [nh, ns), armed by the producer warp as soon as the
 // compute warps release a slot ("empty" mbarrier, one arrival per compute
 // warp).  Compute thread t owns the 16-byte column chunks t, t + kThreads,
 // ... of every row and keeps x of those columns in registers.  Work goes in
-// rounds of up to kGroup neurons:
-//   A. each thread dots its chunks of the round's W1 rows with x; one
-//      transposing butterfly per warp reduces all of them; warp partials go
-//      to shared memory;
-//   B. eight lanes of warp 0 add the kWarps partials in order, add the bias
-//      and apply ReLU (times the up projection, gated);
+// rounds of up to kGroup neurons, one block barrier per round:
+//   A. each thread dots its chunks of the round's W1 rows with x (two fp32
+//      FMA chains per value); one transposing butterfly per warp reduces all of them;
+//      warp partials go to shared memory (double-buffered by round);
+//   -- barrier --
+//   B. every warp adds the kWarps partials of each neuron in the same fixed
+//      tree, adds the bias and applies ReLU (times the up projection, gated):
+//      every warp holds the same h without a second barrier;
 //   C. each thread adds h_q times its chunks of the round's W2 rows.
 // Every sum has a fixed order, so results are deterministic.  A round holds
 // a.grp <= kGroup neurons; a.grp <= ns - nh (no round waits for a slot that
 // only its own release would free), and a shallow ring takes smaller rounds
 // so that copies stay in flight while a round is computed.  lb[k] is b1 of
-// neuron lst[k]; red holds 2 x kGroup x NV x kWarps floats, hbuf 2 x kGroup.
+// neuron lst[k]; red holds 2 x kGroup x NV x kWarps floats (hbuf is unused).
 template <int DT, bool GATED, int NCH>
 __device__ void ffn_ring(const FfnArgs& a, const float* xs, const int* lst, const float* lb, int m,
                          int mh, int nh, unsigned char* slots, uint64_t* full, uint64_t* empty,
@@ -212,6 +232,10 @@ __device__ void ffn_ring(const FfnArgs& a, const float* xs, const int* lst, cons
   const int c = blockIdx.x;
   const int nc = a.ns - nh;
   const int mc = m - mh;
+  // the arguments' fields used in the loops, in registers
+  const int slot_bytes = a.slot_bytes, nch = a.nch, Pg = a.P, dd = a.d;
+  const unsigned long long limit_ns = a.limit_ns;
+  int* const status = a.status;
   volatile int* vbad = bad;
   if (warp == kWarps) {  // producer warp
     if (lane == 0) {
@@ -243,16 +267,36 @@ __device__ void ffn_ring(const FfnArgs& a, const float* xs, const int* lst, cons
     }
     return;
   }
-  __shared__ int s_stop;  // block-uniform decision to abandon the ring
-  const unsigned w1b = (GATED ? 4u : 2u) * (unsigned)a.d;
-  float xr[NCH][8];
+  __shared__ int s_stop[2];  // block-uniform decision to abandon the ring, per round buffer
+  const unsigned w1b = (GATED ? 4u : 2u) * (unsigned)dd;
+  float2 xr[NCH][4];  // x of the thread's columns, in pairs
+  float2 y2[NCH][4];  // the thread's columns of the partial output
   bool colok[NCH];
+  // x of the thread's columns: from shared memory, or (layer-sequence
+  // kernel) from global memory written by other blocks before a grid-wide
+  // wait, read through L2
+  const bool xglob = __isGlobal(xs);
 #pragma unroll
   for (int j = 0; j < NCH; ++j) {
     const int cc = tid + j * kThreads;
-    colok[j] = cc < a.nch;
+    colok[j] = cc < nch;
+    float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
+    if (colok[j]) {
+      const float4* px = reinterpret_cast<const float4*>(xs + 8 * cc);
+      if (xglob) {
+        lo = __ldcg(px);
+        hi = __ldcg(px + 1);
+      } else {
+        lo = px[0];
+        hi = px[1];
+      }
+    }
+    xr[j][0] = make_float2(lo.x, lo.y);
+    xr[j][1] = make_float2(lo.z, lo.w);
+    xr[j][2] = make_float2(hi.x, hi.y);
+    xr[j][3] = make_float2(hi.z, hi.w);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) xr[j][e] = colok[j] ? xs[8 * cc + e] : 0.f;
+    for (int e = 0; e < 4; ++e) y2[j][e] = make_float2(yacc[j][2 * e], yacc[j][2 * e + 1]);
   }
   int cslot = 0, cpar = 0;  // ring position of the next cold entry
   int buf = 0;
@@ -267,7 +311,7 @@ __device__ void ffn_ring(const FfnArgs& a, const float* xs, const int* lst, cons
         const int k = g0 + q;
         unsigned par = 0u;
         if (k < mh) {
-          sl[q] = (lst[k] - c) / a.P;
+          sl[q] = (lst[k] - c) / Pg;
         } else {
           sl[q] = nh + cslot;
           par = (unsigned)cpar;
@@ -276,73 +320,101 @@ __device__ void ffn_ring(const FfnArgs& a, const float* xs, const int* lst, cons
             cpar ^= 1;
           }
         }
-        if (!*vbad && !mbar_wait(full + sl[q], par, a.limit_ns)) {
-          set_status(a.status, PI_ERR_TIMEOUT);
+        // (the flag read once per warp: the wait is a whole-warp call)
+        if (!__any_sync(0xffffffffu, *vbad != 0) &&
+            !mbar_wait_warp(full + sl[q], par, limit_ns)) {
+          if (lane == 0) set_status(status, PI_ERR_TIMEOUT);
           *vbad = 1;
         }
       }
     }
-    // A: partial dot products of the round, one butterfly per warp
+    // A: partial dot products of the round (pairs of fp32 FMAs, two chains
+    // per value), one transposing butterfly per warp, warp partials to
+    // shared memory
     float pd[NR];
 #pragma unroll
     for (int q = 0; q < kGroup; ++q) {
-      float s0 = 0.f, s1 = 0.f;
+      float a0 = 0.f, a1 = 0.f, u0 = 0.f, u1 = 0.f;  // two chains per value
       if (q < kg) {
-        const unsigned char* sp = slots + (size_t)sl[q] * a.slot_bytes;
+        const unsigned char* sp = slots + (size_t)sl[q] * slot_bytes;
 #pragma unroll
         for (int j = 0; j < NCH; ++j) {
           if (colok[j]) {
             const int cc = tid + j * kThreads;
-            float f[8];
-            unpack8<DT>(*reinterpret_cast<const uint4*>(sp + 16 * cc), f);
-            s0 += dot8(f, xr[j]);
+            float2 f[4];
+            unpack4x2<DT>(*reinterpret_cast<const uint4*>(sp + 16 * cc), f);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              a0 = fmaf(f[e].x, xr[j][e].x, a0);
+              a1 = fmaf(f[e].y, xr[j][e].y, a1);
+            }
             if (GATED) {
-              unpack8<DT>(*reinterpret_cast<const uint4*>(sp + 2 * a.d + 16 * cc), f);
-              s1 += dot8(f, xr[j]);
+              unpack4x2<DT>(*reinterpret_cast<const uint4*>(sp + 2 * dd + 16 * cc), f);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                u0 = fmaf(f[e].x, xr[j][e].x, u0);
+                u1 = fmaf(f[e].y, xr[j][e].y, u1);
+              }
             }
           }
         }
       }
-      pd[q * NV] = s0;
-      if (GATED) pd[q * NV + NV - 1] = s1;
+      pd[q * NV] = a0 + a1;
+      if (GATED) pd[q * NV + NV - 1] = u0 + u1;
     }
     const float r = warp_bfly_sum<NR>(pd);
-    float* rb = red + buf * (NR * kWarps);
+    float* rb = red + buf * (NR * kWarps);  // [value][warp]
     if ((lane & (32 / NR - 1)) == 0) rb[bfly_index<NR>(lane) * kWarps + warp] = r;
-    compute_sync();
-    // B: h of the round's neurons
-    float* hb = hbuf + buf * kGroup;
-    if (warp == 0 && lane < kg) {
-      float s0 = 0.f, s1 = 0.f;
-      for (int w = 0; w < kWarps; ++w) {
-        s0 += rb[(lane * NV) * kWarps + w];
-        if (GATED) s1 += rb[(lane * NV + NV - 1) * kWarps + w];
-      }
-      float h = s0 + lb[g0 + lane];
-      h = h > 0.f ? h : 0.f;  // ReLU; ReLU(0) = 0
-      if (GATED) h *= s1;
-      hb[lane] = h;
-    }
     // a wait of this round (or the producer) gave up: every compute warp
     // reads the one decision after the barrier and leaves the ring; the
     // slots are not released, so the producer issues nothing more
-    if (warp == 0 && lane == 0) s_stop = *vbad;
+    if (warp == 0 && lane == 0) s_stop[buf] = *vbad;
     compute_sync();
-    if (s_stop) break;
+    if (s_stop[buf]) break;
+    // B: every warp sums the kWarps partials of each value itself (lane l
+    // holds warp l % 16's partial of values 2i + l / 16, a fixed xor tree
+    // over the 16 warps), so no second barrier is needed; the same
+    // operations in every warp give every warp the same h
+    float hq[kGroup];
+    {
+      constexpr int NL = NR / 2;  // partials per lane
+      float t[NL];
+#pragma unroll
+      for (int i = 0; i < NL; ++i) t[i] = rb[i * 32 + lane];
+#pragma unroll
+      for (int o = 8; o >= 1; o >>= 1)
+#pragma unroll
+        for (int i = 0; i < NL; ++i) t[i] += __shfl_xor_sync(0xffffffffu, t[i], o);
+#pragma unroll
+      for (int q = 0; q < kGroup; ++q) {
+        const int v = q * NV;  // the value of the gate (or of the plain up row)
+        const float s0 = __shfl_sync(0xffffffffu, t[v >> 1], (v & 1) * 16);
+        float h = 0.f;
+        if (q < kg) {
+          h = s0 + lb[g0 + q];
+          h = h > 0.f ? h : 0.f;  // ReLU; ReLU(0) = 0
+        }
+        if constexpr (GATED) h *= __shfl_sync(0xffffffffu, t[(v + 1) >> 1], ((v + 1) & 1) * 16);
+        hq[q] = h;
+      }
+    }
     // C: row-axpy of the round's W2 rows
 #pragma unroll
     for (int q = 0; q < kGroup; ++q) {
       if (q < kg) {
-        const float h = hb[q];
-        const unsigned char* sp = slots + (size_t)sl[q] * a.slot_bytes + w1b;
+        const float2 h2 = make_float2(hq[q], hq[q]);
+        const unsigned char* sp = slots + (size_t)sl[q] * slot_bytes + w1b;
 #pragma unroll
         for (int j = 0; j < NCH; ++j) {
           if (colok[j]) {
             const int cc = tid + j * kThreads;
-            float f[8];
-            unpack8<DT>(*reinterpret_cast<const uint4*>(sp + 16 * cc), f);
+            float2 f[4];
+            unpack4x2<DT>(*reinterpret_cast<const uint4*>(sp + 16 * cc), f);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) yacc[j][e] = fmaf(h, f[e], yacc[j][e]);
+            for (int e = 0; e < 4; ++e) {
+              y2[j][e].x = fmaf(h2.x, f[e].x, y2[j][e].x);
+              y2[j][e].y = fmaf(h2.y, f[e].y, y2[j][e].y);
+            }
           }
         }
       }
@@ -356,6 +428,14 @@ __device__ void ffn_ring(const FfnArgs& a, const float* xs, const int* lst, cons
     }
     buf ^= 1;
   }
+#pragma unroll
+  for (int j = 0; j < NCH; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      yacc[j][2 * e] = y2[j][e].x;
+      yacc[j][2 * e + 1] = y2[j][e].y;
+    }
+  (void)hbuf;
 }
 
 // Sums the P partial rows in a fixed order, adds b2 and the residual, writes

@@ -224,7 +224,8 @@ FfnFn pick_ffn(int dtype, int gated, bool wide) {
 
 // Shared-memory layout of a persistent launch for a given predictor-row
 // placement; returns the bytes before the ring slots (16-byte aligned).
-int layout_fixed(const pi_ffn_desc& D, int mode, int P, int rows_max, int a_in_smem, FfnArgs& a) {
+int layout_fixed(const pi_ffn_desc& D, int mode, int P, int rows_max, int a_in_smem, FfnArgs& a,
+                 bool no_xs = false) {
   int off = 0;
   auto take = [&](int bytes, int align) {
     off = (off + align - 1) / align * align;
@@ -232,7 +233,7 @@ int layout_fixed(const pi_ffn_desc& D, int mode, int P, int rows_max, int a_in_s
     off += bytes;
     return o;
   };
-  a.o_xs = take(4 * D.d, 16);
+  a.o_xs = no_xs ? 0 : take(4 * D.d, 16);  // the layer-sequence kernel reads x from global memory
   a.o_lst = take(4 * (rows_max + kMaxSlots), 16);
   a.o_lb = take(4 * (rows_max + kMaxSlots), 16);
   a.o_red = take(4 * (2 * kGroup * 2 * kWarps + 2 * kGroup + 64), 16);  // butterfly partials, h
@@ -251,7 +252,8 @@ int layout_fixed(const pi_ffn_desc& D, int mode, int P, int rows_max, int a_in_s
 // Fills the shape fields, grid size and shared-memory plan of a persistent
 // launch; returns the dynamic shared-memory bytes, or 0 if the shape does
 // not fit.
-int plan_ffn(const pi_ffn_desc& D, int mode, int P, int positions, int smem_limit, FfnArgs& a) {
+int plan_ffn(const pi_ffn_desc& D, int mode, int P, int positions, int smem_limit, FfnArgs& a,
+             bool no_xs = false) {
   a.d = D.d;
   a.n = D.n;
   a.r = D.r;
@@ -270,11 +272,11 @@ int plan_ffn(const pi_ffn_desc& D, int mode, int P, int positions, int smem_limi
     return ns < kMaxSlots ? ns : kMaxSlots;
   };
   a.a_in_smem = 0;
-  int fixed = layout_fixed(D, mode, P, a.rows_max, 0, a);
+  int fixed = layout_fixed(D, mode, P, a.rows_max, 0, a, no_xs);
   int ns = slots_for(fixed);
   if (mode == kFused) {
     FfnArgs t = a;
-    const int fixed_s = layout_fixed(D, mode, P, a.rows_max, 1, t);
+    const int fixed_s = layout_fixed(D, mode, P, a.rows_max, 1, t, no_xs);
     const int ns_s = slots_for(fixed_s);
     if (ns_s >= 10 || ns_s >= ns) {  // stage A only if the ring stays deep
       a = t;
@@ -282,7 +284,7 @@ int plan_ffn(const pi_ffn_desc& D, int mode, int P, int positions, int smem_limi
       fixed = fixed_s;
       ns = ns_s;
     } else {
-      layout_fixed(D, mode, P, a.rows_max, 0, a);
+      layout_fixed(D, mode, P, a.rows_max, 0, a, no_xs);
     }
   }
   if (ns < 2) return 0;
@@ -901,9 +903,12 @@ pi_status pi_layer_decode(const pi_ffn_desc* desc, const pi_layer_weights* w, co
   s = check_weights(*desc, w, true);
   if (s != PI_OK) return s;
   if (!x || !y || !dev_status || !ws) return PI_ERR_NULL;
-  const void* ps[] = {x, y, residual, idx_out, cnt_out, dev_status, ws};
+  const void* ps[] = {x, y, residual, dev_status, ws};
   for (const void* p : ps)
     if (p && !aligned16(p)) return PI_ERR_ALIGN;
+  // the active lists and counts are written element by element
+  if ((reinterpret_cast<uintptr_t>(idx_out) | reinterpret_cast<uintptr_t>(cnt_out)) & 3u)
+    return PI_ERR_ALIGN;
   const WsLayout L = ws_layout(*desc, batch);
   if (ws_bytes < L.total) return PI_ERR_WORKSPACE;
   const size_t d = (size_t)desc->d, n = (size_t)desc->n;
@@ -981,7 +986,7 @@ pi_status pi_decode_layers(const pi_ffn_desc* descs, const pi_layer_weights* lay
   const bool wide = (D.d / 8) > kThreads;
   SeqFn fn = pick_seq(D.dtype, D.gated, wide);
   FfnArgs a{};
-  const int smem = plan_ffn(D, kFused, P, D.n, di.smem_optin - 1024, a);
+  const int smem = plan_ffn(D, kFused, P, D.n, di.smem_optin - 1024, a, true);
   if (smem == 0 || a.grp < 1) return PI_ERR_SHAPE;
   s = ensure_smem(reinterpret_cast<const void*>(fn), smem);
   if (s != PI_OK) return s;
@@ -1003,6 +1008,12 @@ pi_status pi_decode_layers(const pi_ffn_desc* descs, const pi_layer_weights* lay
   sa.uacc = reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) + L.uacc);
   const int qmax = (D.d / 8 + P - 1) / P;
   sa.bm_smem = (a.nh < a.ns - 1 && D.r * qmax * 16 <= a.slot_bytes) ? 1 : 0;
+  // predictor rows that do not fit beside the ring wait in its idle slots
+  // (after the hot ones, before the Bm slot) between jobs
+  sa.a_slots = (!a.a_in_smem && sa.bm_smem &&
+                (long long)(a.ns - 1 - a.nh) * a.slot_bytes >= (long long)a.rows_max * a.a_stride)
+                   ? 1 : 0;
+  if (const char* e = std::getenv("PI_SEQ_A_SLOTS")) sa.a_slots = sa.a_slots && std::atoi(e) != 0;
   sa.glist = reinterpret_cast<int2*>(static_cast<char*>(ws) + L.glist);
   sa.gcnt = reinterpret_cast<int*>(static_cast<char*>(ws) + L.gcnt);
   sa.balance = 0;  // measured: no gain on the 48-layer stack (its extra wait costs the tail)

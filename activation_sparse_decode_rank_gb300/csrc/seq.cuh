@@ -44,6 +44,25 @@
 namespace pik {
 
 constexpr int kSeqMaxLayers = 128;
+
+struct SeqLayer;
+
+// Block c's share (one P-th, contiguous) of a layer's predictor weights
+// (A [n][r], Bm [r][d], b1 [n]), fetched towards L2 at evict-last priority
+// while the current job's ring streams rows at evict-first priority: the
+// next job then stages its predictor rows from L2.
+__device__ __noinline__ void prefetch_predictor(const void* A, const void* Bm, const float* b1,
+                                                int n, int r, int d, int c, int P) {
+  const char* base[3] = {static_cast<const char*>(A), static_cast<const char*>(Bm),
+                         reinterpret_cast<const char*>(b1)};
+  const unsigned long long size[3] = {(unsigned long long)n * r * 2,
+                                      (unsigned long long)r * d * 2, (unsigned long long)n * 4};
+  for (int k = 0; k < 3; ++k) {
+    const unsigned long long q16 = size[k] / 16;  // whole 16-byte units; a tail is left out
+    const unsigned long long lo = q16 * c / P, hi = q16 * (c + 1) / P;
+    if (hi > lo) prefetch_l2_keep(base[k] + lo * 16, (hi - lo) * 16);
+  }
+}
 constexpr int kSeqMaxQ = 8;  // most own 8-column chunks per block
 
 struct SeqLayer {
@@ -66,6 +85,8 @@ struct SeqArgs {
   unsigned char* mask_out;  // [J][n] or NULL
   unsigned long long* uacc;  // [2][r] fixed-point u, 16 words (128 bytes) apart; zero at launch
   int bm_smem;            // stage the next job's own Bm columns in the last ring slot
+  int a_slots;            // stage the next job's own predictor rows in ring slots [nh, ns - 1)
+                          // (when they do not fit beside the ring)
   int balance;            // spread the cold active neurons evenly (one more grid-wide wait)
   int2* glist;            // [P][rows_max] published cold entries (neuron, b1 bits)
   int* gcnt;              // [P] published cold counts
@@ -76,7 +97,6 @@ template <int DT, bool GATED, int NCH>
 __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
   extern __shared__ __align__(128) unsigned char smem[];
   const FfnArgs& f = sa.f;
-  float* xs = reinterpret_cast<float*>(smem + f.o_xs);
   int* lst = reinterpret_cast<int*>(smem + f.o_lst);
   float* lb = reinterpret_cast<float*>(smem + f.o_lb);
   float* red = reinterpret_cast<float*>(smem + f.o_red);
@@ -84,7 +104,8 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + f.o_mbar);
   uint64_t* empty = full + kMaxSlots;
   unsigned char* slots = smem + f.o_slots;
-  unsigned char* As = smem + f.o_As;
+  // own predictor rows: staged in the fixed region, or in idle ring slots
+  unsigned char* As = sa.a_slots ? slots + (size_t)f.nh * f.slot_bytes : smem + f.o_As;
   float* b1s = reinterpret_cast<float*>(smem + f.o_b1s);
   float* us = reinterpret_cast<float*>(smem + f.o_us);
   unsigned char* flag = smem + f.o_flag;
@@ -100,6 +121,7 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
 
   unsigned char* bms = slots + (size_t)(f.ns - 1) * f.slot_bytes;  // staged Bm columns
   FfnArgs a = f;  // the current job's weights
+  if (sa.a_slots) a.a_in_smem = 1;  // own_logits reads the staged rows
   int nh_c = 0;   // own hot neurons whose rows went to slots for the current job
 
   // The weights of job j that do not depend on its x.  prep_set points the
@@ -107,8 +129,9 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
   // producer lane re-arms the ring barriers (no copy may be in flight) and
   // sends the own hot neurons' rows to their slots; compute threads
   // [t0, t0 + nt) stage the own Bm columns ([k][q], 16 bytes each, in the
-  // last ring slot, a cold one) as one copy group and send the hot rows
-  // beyond the slots towards L2.
+  // last ring slot, a cold one) as one copy group, the own predictor rows
+  // (a_slots: into the idle slots after the hot ones) as a second group,
+  // and send the hot rows beyond the slots towards L2.
   bool armed = false;  // the ring barriers hold a previous job's state
   auto prep_set = [&](int j) {
     const SeqLayer& Lw = sa.L[j % sa.R];
@@ -145,15 +168,27 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
           cp_async16(bms + (size_t)e * 16, a.Bm + (size_t)k * f.d + 8 * (q0 + q));
         }
       cp_async_commit();
+      if (sa.a_slots) {
+        const int rc = a.r >> 3;
+        for (int e = t; e < rows * rc; e += nt) {
+          const int jj = e / rc, q = e - jj * rc;
+          cp_async16(As + (size_t)jj * f.a_stride + 16 * q,
+                     a.A + ((size_t)c + (size_t)jj * P) * a.r + 8 * q);
+        }
+      }
+      cp_async_commit();
       for (int k = nh_c + t; k < hot_own; k += nt) prefetch_neuron<GATED>(a, c + k * P);
     }
   };
+
   // The job's predictor rows (staged, or towards L2) and biases: issued by
   // every compute thread once the block has arrived at the first grid-wide
   // wait (they are first read by the logits, after it), one copy group.
   auto rows_issue = [&]() {
     if (compute) {
-      if (f.a_in_smem) {
+      if (sa.a_slots) {
+        // staged at the job's start (prep_issue)
+      } else if (f.a_in_smem) {
         const int rc = a.r >> 3;
         for (int e = tid; e < rows * rc; e += kThreads) {
           const int jj = e / rc, q = e - jj * rc;
@@ -249,15 +284,7 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
     // own columns of this job's x: job 0 reads them here; later jobs find
     // them in xo (written by the previous job's R phase)
     if (j == 0 && tid < nq * 8) xo[tid] = __ldcg(sa.x + 8 * q0 + tid);
-    // independent steps: the whole x of this job goes to shared memory now,
-    // its transfer overlapping stage 1 and the first grid-wide wait (a
-    // chained job's x is complete only after that wait); one copy group in
-    // either case, so the group counts below hold for both
-    if (!sa.chain)
-      for (int i = tid; i < (f.d >> 2); i += kBlock)
-        cp_async16(xs + 4 * i, sa.x + (size_t)j * f.d + 4 * i);
-    cp_async_commit();
-    cp_async_wait_group<1>();  // this job's staged Bm columns (x may still land)
+    cp_async_wait_group<1>();  // this job's staged Bm columns (its predictor rows may still land)
     __syncthreads();
     if (ov && j > 0) reduce_cols(j - 1, b2prev);
     // U: partial predictor stage 1 over the own columns, u_c[k] for k < r
@@ -307,12 +334,7 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
       bail();
       return;
     }
-    // L: the whole x (chained), u, own logits and list
-    if (sa.chain) {
-      const float* xj = j == 0 ? sa.x : sa.y + (size_t)(j - 1) * f.d;
-      for (int i = tid; i < (f.d >> 2); i += kBlock)
-        reinterpret_cast<float4*>(xs)[i] = __ldcg(reinterpret_cast<const float4*>(xj) + i);
-    }
+    // L: u, own logits and list
     if (tid < f.r) {
       // u[k] from its accumulator; block 0 clears the other buffer (last
       // read by the previous job, before this job's first wait) for the
@@ -323,7 +345,10 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
       }
       if (c == 0) sa.uacc[((size_t)((j + 1) & 1) * f.r + tid) * 16] = 0ull;
     }
-    cp_async_wait_all();  // this job's staged predictor rows, biases (and x)
+    cp_async_wait_all();  // this job's staged predictor rows and biases
+    // the staging wrote ring slots through the generic proxy; the ring's
+    // bulk copies (async proxy) write them again later
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
     if (compute) own_logits<DT>(a, As, b1s, us, flag, rows);
     __syncthreads();
@@ -436,7 +461,15 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
     for (int q = 0; q < NCH; ++q)
 #pragma unroll
       for (int e = 0; e < 8; ++e) yacc[q][e] = 0.f;
-    ffn_ring<DT, GATED, NCH>(a, xs, lst, lb, m, mh, f.nh, slots, full, empty, red,
+    if (tid == 0 && j + 1 < sa.J) {
+      const SeqLayer& Ln = sa.L[(j + 1) % sa.R];
+      prefetch_predictor(Ln.A, Ln.Bm, Ln.b1, f.n, Ln.r, f.d, c, P);
+    }
+    // the job's whole x, read by the ring from global memory (a chained
+    // job's x is complete only after the first grid-wide wait)
+    const float* xg = sa.chain ? (j == 0 ? sa.x : sa.y + (size_t)(j - 1) * f.d)
+                               : sa.x + (size_t)j * f.d;
+    ffn_ring<DT, GATED, NCH>(a, xg, lst, lb, m, mh, f.nh, slots, full, empty, red,
                              red + 2 * kGroup * 2 * kWarps, yacc, &s_bad);
     __syncthreads();
     // copies of own hot neurons that turned out inactive land before the

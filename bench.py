@@ -877,6 +877,7 @@ def run_sweep(args):
                 "dense_gbs": dense_alg / res["dense"] / 1e3,
                 "dense_frac": dense_alg / res["dense"] / 1e3 / peak,
                 "plan": sweep_plan(pi, desc, B, pz, res),
+                "dispatched": sweep_dispatched(pi, torch, desc, wts[0], xs[0], B, pz, K, stream),
             })
             del xs, ws
         del reps, wts, base
@@ -910,6 +911,43 @@ def run_sweep(args):
         "clocks": clocks, "csrc_hash": csrc_hash(),
     }), flush=True)
     return 0
+
+
+def sweep_dispatched(pi, torch, desc, w, x, B, pz, K, stream):
+    """The step as a user runs it through the plan's executor: a pi_decoder
+    (the generator's p_i as its profile, dense allowed) bound to fixed
+    buffers, one graph launch per step; the path it chose and its measured
+    microseconds per step."""
+    d = desc.d
+    dev = x.device
+    xb = torch.zeros((32, d), dtype=torch.float32, device=dev)
+    xb[:B].copy_(x)
+    yb = torch.empty((32, d), dtype=torch.float32, device=dev)
+    st = torch.zeros(4, dtype=torch.int32, device=dev)
+    ws = pi.workspace(desc, 32, dev)
+    rc, dec = pi.pi_decoder_create(desc, w, pz.astype(np.float32), 0.0, 1, None, xb, yb, None, st,
+                                   ws)
+    pi.check(rc, "pi_decoder_create")
+    try:
+        plan = pi.pi_plan()
+        pi.check(pi.pi_decoder_plan(dec, B, plan))
+        with torch.cuda.stream(stream):
+            for _ in range(3):  # the first run captures the graph
+                pi.check(pi.pi_decoder_run(dec, B, stream=stream))
+            stream.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(K):
+                pi.check(pi.pi_decoder_run(dec, B, stream=stream))
+            e1.record(stream)
+            stream.synchronize()
+        if int(st[0]) != 0:
+            raise SystemExit(f"bench: device status {pi.status_string(int(st[0]))}")
+        return {"path": pi.PATH_NAMES[plan.path], "us": e0.elapsed_time(e1) / K * 1e3,
+                "how": "pi_decoder_run: one graph launch per step (one weight copy)"}
+    finally:
+        pi.pi_decoder_destroy(dec)
 
 
 def sweep_plan(pi, desc, B, pz, res):

@@ -201,8 +201,9 @@ pi_status pi_dense_ffn(const pi_ffn_desc* desc, const pi_layer_weights* w,
  *     y[t] = (residual ? residual[t] : 0) + FFN_sparse(x[t])
  * residual may be NULL; pass residual = x for a residual stack.  idx_out
  * ([batch][n]) and cnt_out ([batch]) may be NULL; when given they receive
- * each token's ascending active list and count.  dev_status must not be
- * NULL. */
+ * each token's ascending active list and count (for batch 1 and for
+ * batches that run token by token these two need only 4-byte alignment;
+ * the batched union path needs 16).  dev_status must not be NULL. */
 pi_status pi_layer_decode(const pi_ffn_desc* desc, const pi_layer_weights* w,
                           const float* x, int32_t batch, float* y,
                           const float* residual, int32_t* idx_out,

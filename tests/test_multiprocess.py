@@ -105,3 +105,60 @@ def test_stack_oracle_sample_walks_every_layer_on_the_host():
     x = synth.gen_x(9, 0, 1, 64)[0]
     assert np.array_equal(oracle.layer_decode(H, x, residual=True)[3],
                           oracle.layer_decode(hosts[1], x, residual=True)[3])
+
+
+def _shard_worker(rank, world, port, q):
+    # one rank of a neuron-sharded layer on the CPU: the rank's partial
+    # output is the oracle's over its own neurons (g, g + G, ...), the
+    # exchange is the library's all-gather helper over gloo, and the sum
+    # runs in rank order
+    import torch
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import activation_sparse_decode_rank_gb300 as pi
+    from activation_sparse_decode_rank_gb300 import sharded
+    import oracle
+    import synth
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
+                            world_size=world)
+    try:
+        d, n, r, hot = 96, 301, 16, 40
+        L = synth.make_layer(d, n, r, "f16", alpha=0.9, density=0.15, seed=61)
+        desc = pi.make_desc(d, n, r, "f16", False, hot)
+        sd = sharded.shard_desc(desc, world, rank)
+        rows = np.arange(rank, n, world)
+        assert sd.n == len(rows) and sd.hot_prefix == int((rows < hot).sum())
+        part_layer = synth.Layer(d, sd.n, r, "f16", False, np.ascontiguousarray(L.A[rows]), L.Bm,
+                                 np.ascontiguousarray(L.b1[rows]), np.ascontiguousarray(L.W1[rows]),
+                                 np.ascontiguousarray(L.W2[rows]),
+                                 L.b2 if rank == 0 else np.zeros_like(L.b2), {})
+        x = synth.gen_x(62, 0, 1, d)[0]
+        _, idx, y, _ = oracle.layer_decode(part_layer, x)
+        parts = sharded.exchange(torch.from_numpy(y.reshape(1, d)), world)
+        lists = [None] * world
+        dist.all_gather_object(lists, (rows[idx]).tolist())
+        ysum = np.zeros(d)
+        for g in range(world):  # rank order
+            ysum = ysum + parts[g, 0].numpy()
+        _, gidx, yfull, _ = oracle.layer_decode(L, x)
+        merged = sorted(v for lst in lists for v in lst)
+        q.put((rank, merged == gidx.tolist(), float(np.abs(ysum - yfull).max()),
+               float(np.abs(yfull).max())))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_sharded_layer_gloo_two_ranks_matches_the_whole_layer():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_shard_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = sorted(q.get(timeout=180) for _ in range(2))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, same_set, diff, scale in out:
+        assert same_set                   # the shards' lists partition the active set
+        assert diff <= 1e-12 * scale      # partial sums in rank order: fp64 rounding only
