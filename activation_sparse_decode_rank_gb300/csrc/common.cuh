@@ -50,18 +50,6 @@ __device__ __forceinline__ void unpack8(const uint4& v, float f[8]) {
   }
 }
 
-// Two fp32 fused multiply-adds in one instruction: d = a * b + c per lane
-// of the pair, each rounded once (the same result as two fmaf calls).
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-  unsigned long long d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;"
-      : "=l"(d)
-      : "l"(*reinterpret_cast<unsigned long long*>(&a)),
-        "l"(*reinterpret_cast<unsigned long long*>(&b)),
-        "l"(*reinterpret_cast<unsigned long long*>(&c)));
-  return *reinterpret_cast<float2*>(&d);
-}
-
 // Converts 8 packed 16-bit values (fp16 if DT == 0, bf16 if DT == 1) to four
 // fp32 pairs (elements 2i, 2i + 1 in pair i).
 template <int DT>
@@ -230,19 +218,12 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* m, unsigned bytes) {
                : "memory");
 }
 
-// L2 eviction priorities for data read once (streamed weight rows) and for
-// data fetched early that must survive the stream until it is read.
+// L2 eviction priority for data read once (streamed weight rows).
 __device__ __forceinline__ uint64_t l2_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
-__device__ __forceinline__ uint64_t l2_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
 // One-dimensional bulk copy global -> shared (TMA unit), completing on `m`,
 // with the source lines marked evict-first in L2 (streamed once).
 // Addresses 16-byte aligned, size a multiple of 16.
@@ -252,21 +233,6 @@ __device__ __forceinline__ void bulk_g2s(void* sdst, const void* gsrc, unsigned 
       "%2, [%3], %4;" ::"r"(smem_u32(sdst)),
       "l"(gsrc), "r"(bytes), "r"(smem_u32(m)), "l"(l2_evict_first())
       : "memory");
-}
-
-// Bulk prefetch of [p, p + bytes) into L2 at evict-last priority (no
-// completion to wait on); p 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void prefetch_l2_keep(const void* p, unsigned long long bytes) {
-  const char* c = static_cast<const char*>(p);
-  const uint64_t pol = l2_evict_last();
-  while (bytes > 0) {
-    const unsigned chunk = bytes > (1u << 20) ? (1u << 20) : (unsigned)bytes;
-    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(c),
-                 "r"(chunk), "l"(pol)
-                 : "memory");
-    c += chunk;
-    bytes -= chunk;
-  }
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* m, unsigned parity) {
@@ -303,28 +269,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* m, unsigned parity, uint64_t
   while (!mbar_try_wait(m, parity))
     if (global_ns() - t0 > limit_ns) return false;
   return true;
-}
-
-// The same for a whole warp: lane 0 polls (the timer read once per 32
-// polls), then the warp observes the completed phase; every lane returns
-// the same answer.  Call with all 32 lanes.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t* m, unsigned parity, uint64_t limit_ns) {
-  int ok = 1;
-  if ((threadIdx.x & 31) == 0 && !mbar_test(m, parity)) {
-    const uint64_t t0 = global_ns();
-    unsigned spins = 0;
-    while (!mbar_try_wait(m, parity)) {
-      if ((++spins & 31u) == 0u && global_ns() - t0 > limit_ns) {
-        ok = 0;
-        break;
-      }
-    }
-  }
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  // every lane observes the phase itself (acquire for its own later reads
-  // of the slot); at once when lane 0 saw it complete
-  if (ok) ok = mbar_test(m, parity) ? 1 : 0;
-  return __all_sync(0xffffffffu, ok) != 0;
 }
 
 // The same for a thread that only waits (the producer warp): sleeps between

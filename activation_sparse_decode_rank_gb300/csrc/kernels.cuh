@@ -208,20 +208,18 @@ __device__ __forceinline__ void own_logits(const FfnArgs& a, const unsigned char
 // compute warps release a slot ("empty" mbarrier, one arrival per compute
 // warp).  Compute thread t owns the 16-byte column chunks t, t + kThreads,
 // ... of every row and keeps x of those columns in registers.  Work goes in
-// rounds of up to kGroup neurons, one block barrier per round:
+// rounds of up to kGroup neurons:
 //   A. each thread dots its chunks of the round's W1 rows with x (two fp32
-//      FMA chains per value); one transposing butterfly per warp reduces all of them;
-//      warp partials go to shared memory (double-buffered by round);
-//   -- barrier --
-//   B. every warp adds the kWarps partials of each neuron in the same fixed
-//      tree, adds the bias and applies ReLU (times the up projection, gated):
-//      every warp holds the same h without a second barrier;
+//      FMA chains per value); one transposing butterfly per warp reduces all
+//      of them; warp partials go to shared memory (double-buffered by round);
+//   B. eight lanes of warp 0 add the kWarps partials in order, add the bias
+//      and apply ReLU (times the up projection, gated);
 //   C. each thread adds h_q times its chunks of the round's W2 rows.
 // Every sum has a fixed order, so results are deterministic.  A round holds
 // a.grp <= kGroup neurons; a.grp <= ns - nh (no round waits for a slot that
 // only its own release would free), and a shallow ring takes smaller rounds
 // so that copies stay in flight while a round is computed.  lb[k] is b1 of
-// neuron lst[k]; red holds 2 x kGroup x NV x kWarps floats (hbuf is unused).
+// neuron lst[k]; red holds 2 x kGroup x NV x kWarps floats, hbuf 2 x kGroup.
 template <int DT, bool GATED, int NCH>
 __device__ void ffn_ring(const FfnArgs& a, const float* xs, const int* lst, const float* lb, int m,
                          int mh, int nh, unsigned char* slots, uint64_t* full, uint64_t* empty,
@@ -320,10 +318,8 @@ __device__ void ffn_ring(const FfnArgs& a, const float* xs, const int* lst, cons
             cpar ^= 1;
           }
         }
-        // (the flag read once per warp: the wait is a whole-warp call)
-        if (!__any_sync(0xffffffffu, *vbad != 0) &&
-            !mbar_wait_warp(full + sl[q], par, limit_ns)) {
-          if (lane == 0) set_status(status, PI_ERR_TIMEOUT);
+        if (!*vbad && !mbar_wait(full + sl[q], par, limit_ns)) {
+          set_status(status, PI_ERR_TIMEOUT);
           *vbad = 1;
         }
       }
@@ -368,35 +364,31 @@ __device__ void ffn_ring(const FfnArgs& a, const float* xs, const int* lst, cons
     // a wait of this round (or the producer) gave up: every compute warp
     // reads the one decision after the barrier and leaves the ring; the
     // slots are not released, so the producer issues nothing more
-    if (warp == 0 && lane == 0) s_stop[buf] = *vbad;
     compute_sync();
-    if (s_stop[buf]) break;
-    // B: every warp sums the kWarps partials of each value itself (lane l
-    // holds warp l % 16's partial of values 2i + l / 16, a fixed xor tree
-    // over the 16 warps), so no second barrier is needed; the same
-    // operations in every warp give every warp the same h
+    // B: h of the round's neurons, eight lanes of warp 0 adding the kWarps
+    // partials in order; every warp reads them after the second barrier
     float hq[kGroup];
     {
-      constexpr int NL = NR / 2;  // partials per lane
-      float t[NL];
-#pragma unroll
-      for (int i = 0; i < NL; ++i) t[i] = rb[i * 32 + lane];
-#pragma unroll
-      for (int o = 8; o >= 1; o >>= 1)
-#pragma unroll
-        for (int i = 0; i < NL; ++i) t[i] += __shfl_xor_sync(0xffffffffu, t[i], o);
-#pragma unroll
-      for (int q = 0; q < kGroup; ++q) {
-        const int v = q * NV;  // the value of the gate (or of the plain up row)
-        const float s0 = __shfl_sync(0xffffffffu, t[v >> 1], (v & 1) * 16);
-        float h = 0.f;
-        if (q < kg) {
-          h = s0 + lb[g0 + q];
-          h = h > 0.f ? h : 0.f;  // ReLU; ReLU(0) = 0
+      float* hb = hbuf + buf * kGroup;
+      if (warp == 0 && lane < kg) {
+        float s0 = 0.f, s1 = 0.f;
+        for (int w = 0; w < kWarps; ++w) {
+          s0 += rb[(lane * NV) * kWarps + w];
+          if (GATED) s1 += rb[(lane * NV + NV - 1) * kWarps + w];
         }
-        if constexpr (GATED) h *= __shfl_sync(0xffffffffu, t[(v + 1) >> 1], ((v + 1) & 1) * 16);
-        hq[q] = h;
+        float h = s0 + lb[g0 + lane];
+        h = h > 0.f ? h : 0.f;
+        if (GATED) h *= s1;
+        hb[lane] = h;
       }
+      // a wait of this round (or the producer) gave up: every compute warp
+      // reads the one decision after the barrier and leaves the ring; the
+      // slots are not released, so the producer issues nothing more
+      if (warp == 0 && lane == 0) s_stop[buf] = *vbad;
+      compute_sync();
+      if (s_stop[buf]) break;
+#pragma unroll
+      for (int q = 0; q < kGroup; ++q) hq[q] = hb[q];
     }
     // C: row-axpy of the round's W2 rows
 #pragma unroll
@@ -435,7 +427,6 @@ __device__ void ffn_ring(const FfnArgs& a, const float* xs, const int* lst, cons
       yacc[j][2 * e] = y2[j][e].x;
       yacc[j][2 * e + 1] = y2[j][e].y;
     }
-  (void)hbuf;
 }
 
 // Sums the P partial rows in a fixed order, adds b2 and the residual, writes

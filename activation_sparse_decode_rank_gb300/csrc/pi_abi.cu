@@ -297,10 +297,12 @@ int plan_ffn(const pi_ffn_desc& D, int mode, int P, int positions, int smem_limi
     if (a.nh < 0) a.nh = 0;
   }
   if (a.ns < 8) a.nh = 0;  // shallow ring: keep every slot for the active rows
-  // rounds of kGroup neurons need two rounds of cold slots to keep copies in
-  // flight; a shallower ring takes rounds of 2 (or 1)
+  // rounds of up to kGroup neurons: larger rounds cost less per neuron (the
+  // round's barriers and reductions are shared), as long as enough slots stay
+  // in flight while a round is computed (measured on the OPT-30B shape with 7
+  // cold slots: 3 neurons per round 31.2 us per layer, 4: 33.0, 2: 42)
   const int nc = a.ns - a.nh;
-  a.grp = nc >= 2 * kGroup ? kGroup : (nc >= 4 ? 2 : 1);
+  a.grp = nc >= 10 ? kGroup : (nc >= 6 ? 3 : (nc >= 4 ? 2 : 1));
   a.o_slots = fixed;
   return fixed + ns * a.slot_bytes;
 }

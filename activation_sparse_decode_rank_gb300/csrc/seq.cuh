@@ -44,25 +44,6 @@
 namespace pik {
 
 constexpr int kSeqMaxLayers = 128;
-
-struct SeqLayer;
-
-// Block c's share (one P-th, contiguous) of a layer's predictor weights
-// (A [n][r], Bm [r][d], b1 [n]), fetched towards L2 at evict-last priority
-// while the current job's ring streams rows at evict-first priority: the
-// next job then stages its predictor rows from L2.
-__device__ __noinline__ void prefetch_predictor(const void* A, const void* Bm, const float* b1,
-                                                int n, int r, int d, int c, int P) {
-  const char* base[3] = {static_cast<const char*>(A), static_cast<const char*>(Bm),
-                         reinterpret_cast<const char*>(b1)};
-  const unsigned long long size[3] = {(unsigned long long)n * r * 2,
-                                      (unsigned long long)r * d * 2, (unsigned long long)n * 4};
-  for (int k = 0; k < 3; ++k) {
-    const unsigned long long q16 = size[k] / 16;  // whole 16-byte units; a tail is left out
-    const unsigned long long lo = q16 * c / P, hi = q16 * (c + 1) / P;
-    if (hi > lo) prefetch_l2_keep(base[k] + lo * 16, (hi - lo) * 16);
-  }
-}
 constexpr int kSeqMaxQ = 8;  // most own 8-column chunks per block
 
 struct SeqLayer {
@@ -461,10 +442,6 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
     for (int q = 0; q < NCH; ++q)
 #pragma unroll
       for (int e = 0; e < 8; ++e) yacc[q][e] = 0.f;
-    if (tid == 0 && j + 1 < sa.J) {
-      const SeqLayer& Ln = sa.L[(j + 1) % sa.R];
-      prefetch_predictor(Ln.A, Ln.Bm, Ln.b1, f.n, Ln.r, f.d, c, P);
-    }
     // the job's whole x, read by the ring from global memory (a chained
     // job's x is complete only after the first grid-wide wait)
     const float* xg = sa.chain ? (j == 0 ? sa.x : sa.y + (size_t)(j - 1) * f.d)
