@@ -220,10 +220,24 @@ __device__ __forceinline__ void own_logits(const FfnArgs& a, const unsigned char
 // only its own release would free), and a shallow ring takes smaller rounds
 // so that copies stay in flight while a round is computed.  lb[k] is b1 of
 // neuron lst[k]; red holds 2 x kGroup x NV x kWarps floats, hbuf 2 x kGroup.
+// After the ring was abandoned (s_bad): the producer's last copy into each
+// cold slot (iss[0]: slots with a copy, iss[1]: the parity of its phase)
+// lands before the slots are re-armed or the block exits; bounded by
+// drain_ns.  Not needed on the normal path, where the compute warps waited
+// for every copy issued.
+__device__ __forceinline__ void ring_drain(uint64_t* full, int nh, int nc, const unsigned* iss,
+                                           unsigned long long drain_ns, int* status) {
+  const unsigned issued = iss[0], par = iss[1];
+  for (int q = 0; q < nc; ++q)
+    if (((issued >> q) & 1u) && !mbar_wait_sleep(full + nh + q, (par >> q) & 1u, drain_ns))
+      set_status(status, PI_ERR_TIMEOUT);
+}
+
 template <int DT, bool GATED, int NCH>
 __device__ void ffn_ring(const FfnArgs& a, const float* xs, const int* lst, const float* lb, int m,
                          int mh, int nh, unsigned char* slots, uint64_t* full, uint64_t* empty,
-                         float* red, float* hbuf, float (&yacc)[NCH][8], int* bad) {
+                         float* red, float* hbuf, float (&yacc)[NCH][8], int* bad,
+                         unsigned* iss) {
   constexpr int NV = GATED ? 2 : 1;
   constexpr int NR = kGroup * NV;  // values reduced per round
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -242,7 +256,8 @@ __device__ void ffn_ring(const FfnArgs& a, const float* xs, const int* lst, cons
       unsigned issued = 0u, par = 0u;
       for (int kc = 0; kc < mc; ++kc) {
         const int s = nh + kc % nc;
-        if (*vbad) break;  // the compute warps gave up: issue nothing more
+        // (compute warps that gave up release no slot: this wait then ends
+        // at its own bound)
         if (kc >= nc &&
             !mbar_wait_sleep(empty + s, (unsigned)((kc / nc - 1) & 1), a.limit_ns)) {
           set_status(a.status, PI_ERR_TIMEOUT);
@@ -254,14 +269,10 @@ __device__ void ffn_ring(const FfnArgs& a, const float* xs, const int* lst, cons
         issued |= 1u << (s - nh);
         par = (par & ~(1u << (s - nh))) | ((unsigned)((kc / nc) & 1) << (s - nh));
       }
-      // every copy issued lands before the slots are re-armed or the block
-      // exits (at once on the normal path: the compute warps consumed them)
-      for (int q = 0; q < nc; ++q)
-        if (((issued >> q) & 1u) &&
-            !mbar_wait_sleep(full + nh + q, (par >> q) & 1u, a.drain_ns)) {
-          set_status(a.status, PI_ERR_TIMEOUT);
-          *vbad = 1;
-        }
+      // on the normal path the compute warps waited for every copy issued;
+      // after a give-up, ring_drain waits for these before the block exits
+      iss[0] = issued;
+      iss[1] = par;
     }
     return;
   }
@@ -318,7 +329,7 @@ __device__ void ffn_ring(const FfnArgs& a, const float* xs, const int* lst, cons
             cpar ^= 1;
           }
         }
-        if (!*vbad && !mbar_wait(full + sl[q], par, limit_ns)) {
+        if (!mbar_wait(full + sl[q], par, limit_ns)) {
           set_status(status, PI_ERR_TIMEOUT);
           *vbad = 1;
         }
@@ -533,6 +544,7 @@ __global__ void __launch_bounds__(kBlock, 1) ffn_kernel(const FfnArgs a) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool compute = tid < kThreads;
   __shared__ int s_m, s_mh, s_bad;
+  __shared__ unsigned s_iss[2];  // the ring producer's issued slots and their phase parities
   __shared__ unsigned long long s_base;
 
   const int hot_own = (MODE == kFused && c < a.hot) ? (a.hot - 1 - c) / P + 1 : 0;
@@ -744,9 +756,11 @@ __global__ void __launch_bounds__(kBlock, 1) ffn_kernel(const FfnArgs a) {
   for (int j = 0; j < NCH; ++j)
 #pragma unroll
     for (int e = 0; e < 8; ++e) yacc[j][e] = 0.f;
+  if (tid == kThreads) s_iss[0] = s_iss[1] = 0u;
   ffn_ring<DT, GATED, NCH>(a, xs, lst, lb, m, mh, nh, slots, full, empty, red,
-                           red + 2 * kGroup * 2 * kWarps, yacc, &s_bad);
+                           red + 2 * kGroup * 2 * kWarps, yacc, &s_bad, s_iss);
   __syncthreads();
+  if (s_bad && tid == kThreads) ring_drain(full, nh, a.ns - nh, s_iss, a.drain_ns, a.status);
   // speculative copies of own hot neurons that turned out inactive must land
   // before the block may exit
   if (MODE == kFused && tid == kThreads && mh < nh_c) {

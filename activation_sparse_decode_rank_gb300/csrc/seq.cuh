@@ -94,6 +94,7 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool compute = tid < kThreads;
   __shared__ int s_m, s_mh, s_bad;
+  __shared__ unsigned s_iss[2];  // the ring producer's issued slots and their phase parities
   __shared__ unsigned long long s_base;
 
   const int rows = (c < f.n) ? (f.n - 1 - c) / P + 1 : 0;  // own neurons c, c + P, ...
@@ -446,8 +447,9 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
     // job's x is complete only after the first grid-wide wait)
     const float* xg = sa.chain ? (j == 0 ? sa.x : sa.y + (size_t)(j - 1) * f.d)
                                : sa.x + (size_t)j * f.d;
+    if (tid == kThreads) s_iss[0] = s_iss[1] = 0u;
     ffn_ring<DT, GATED, NCH>(a, xg, lst, lb, m, mh, f.nh, slots, full, empty, red,
-                             red + 2 * kGroup * 2 * kWarps, yacc, &s_bad);
+                             red + 2 * kGroup * 2 * kWarps, yacc, &s_bad, s_iss);
     __syncthreads();
     // copies of own hot neurons that turned out inactive land before the
     // slots are re-armed
@@ -461,6 +463,7 @@ __global__ void __launch_bounds__(kBlock, 1) seq_kernel(const SeqArgs sa) {
     nh_c = 0;  // every slot copy of this job has landed
     __syncthreads();
     if (s_bad) {  // a ring wait gave up (block-uniform after the barrier)
+      if (tid == kThreads) ring_drain(full, f.nh, f.ns - f.nh, s_iss, f.drain_ns, f.status);
       cp_async_wait_all();
       __syncthreads();
       return;
