@@ -1,7 +1,9 @@
 // pi_abi.cu — host side of the libpi C ABI (declared in include/pi.h):
 // argument validation, workspace layout, launch configuration.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstdlib>
 #include <mutex>
@@ -14,6 +16,7 @@
 #include "seq.cuh"
 #include "plan.cuh"
 #include "tc.cuh"
+#include "tcd.cuh"
 
 using namespace pik;
 
@@ -76,7 +79,10 @@ WsLayout ws_layout(const pi_ffn_desc& D, int batch) {
     L.xlo = take(2 * (size_t)L.bp * D.d);
     L.hhi = take(2 * (size_t)L.bp * L.hs);
     L.hlo = take(2 * (size_t)L.bp * L.hs);
-    L.bpart = take(sizeof(float) * (size_t)kGroups2 * L.bp * D.d);
+    // phase-2 partials: [kGroups2][bp][d] (mma.sync phases) or [P][2][bp][128]
+    // (tensor-memory phases of the dense FFN)
+    const size_t pg = (size_t)kGroups2 * L.bp * D.d, pt = (size_t)kPMax * 2 * L.bp * 128;
+    L.bpart = take(sizeof(float) * (pg > pt ? pg : pt));
     L.ppart = take(sizeof(float) * (size_t)kPMax * batch * D.r);  // predictor partials [G][batch][r]
     L.uhi = take(2 * (size_t)L.bp * D.r);
     L.ulo = take(2 * (size_t)L.bp * D.r);
@@ -367,6 +373,148 @@ void bind_weights(FfnArgs& a, const pi_layer_weights& w) {
   a.b2 = w.b2;
 }
 
+// ------------------------------------------------------------ tensor maps
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link to the
+// driver library).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+bool g_encode_tried = false;
+
+EncodeTiledFn encode_fn() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode_tried) {
+    g_encode_tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return g_encode;
+}
+
+// Map over a row-major matrix of 16-bit elements (rows x inner, row pitch
+// `pitch` elements): boxes of 64 elements x box_rows rows, 128-byte swizzle,
+// rows past the end read as zero.
+bool make_map(CUtensorMap* m, const void* base, size_t inner, size_t rows, size_t pitch,
+              unsigned box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)pitch * 2};
+  const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+  const cuuint32_t es[2] = {1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// PI_BATCH_LEGACY=1 runs the dense batched FFN on the mma.sync phases
+// instead of the tensor-memory ones (read once per process).
+int g_batch_legacy = -1;
+bool batch_legacy() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_batch_legacy < 0) {
+    const char* e = std::getenv("PI_BATCH_LEGACY");
+    g_batch_legacy = (e && std::atoi(e) != 0) ? 1 : 0;
+  }
+  return g_batch_legacy == 1;
+}
+
+// The dense batched FFN (all n neurons, every token) on the tcgen05 / TMA
+// phases of tcd.cuh, x already split into its high / low parts.  Sets *used
+// = false, launching nothing, where the shape does not fit them (d % 128,
+// n % 64, more column tiles than blocks) or PI_BATCH_LEGACY is set.
+pi_status launch_td(const pi_ffn_desc& D, const BatchArgs& a, const DevInfo& di, cudaStream_t st,
+                    bool* used) {
+  *used = false;
+  if (batch_legacy()) return PI_OK;
+  const int P = di.sms;
+  const int NW = D.gated ? 2 : 1;
+  if (D.d % 128 != 0 || D.n % 64 != 0) return PI_OK;
+  const int nct = D.d / 128, nkb = D.n / 64;
+  if (nct > P || (long long)nct * nkb < P) return PI_OK;
+  // the high and low parts of x and of H^T are read as one [2 bp][...] box
+  if (a.xlo != a.xhi + (size_t)a.bp * D.d || a.hlo != a.hhi + (size_t)a.bp * a.hs) return PI_OK;
+  TdArgs t{};
+  t.d = D.d;
+  t.n = D.n;
+  t.batch = a.batch;
+  t.bp = a.bp;
+  t.P = P;
+  const int ng = D.n / 8;
+  const int rmax = 8 * ((ng + P - 1) / P);  // most rows of a block
+  if (rmax > 256) return PI_OK;              // one accumulator tile per block
+  const int bp2 = 2 * a.bp;
+  const int budget = di.smem_optin - 2048;  // static shared memory and the 1024-byte alignment
+  t.wrows = rmax;
+  t.ncol1 = (int)round_up((size_t)rmax, 16);
+  t.stage1 = kTdHalf + NW * t.wrows * 128;
+  // the last stage's last B read may run (ncol1 - wrows) rows past it
+  const int guard1 = (int)round_up((size_t)(t.ncol1 - t.wrows) * 128, 1024);
+  t.ns1 = std::min(kTdMaxStages, (budget - guard1) / t.stage1);
+  t.stage2 = (int)round_up((size_t)2 * 64 * 128 + (size_t)bp2 * 128, 1024);
+  t.ns2 = std::min(kTdMaxStages, budget / t.stage2);
+  if (t.ns1 < 2 || t.ns2 < 2) return PI_OK;
+  // the phase-1 epilogue's staging of the accumulators fits in the stages
+  if ((size_t)NW * bp2 * (t.ncol1 + 4) * sizeof(float) > (size_t)t.ns1 * t.stage1) return PI_OK;
+  auto pow2 = [](int v) {
+    int p = 32;
+    while (p < v) p <<= 1;
+    return p;
+  };
+  t.tcols1 = pow2(NW * t.ncol1);
+  t.tcols2 = pow2(2 * bp2);
+  if (t.tcols1 > 512) return PI_OK;
+  t.hs = a.hs;
+  t.nct = nct;
+  t.nkb = nkb;
+  const size_t w1row = a.packed ? (size_t)a.rec : (size_t)NW * D.d;
+  const size_t w2row = a.packed ? (size_t)a.rec : (size_t)D.d;
+  t.w2x = a.packed ? NW * D.d : 0;
+  t.b1 = a.b1;
+  t.b2 = a.b2;
+  t.residual = a.residual;
+  t.y = a.y;
+  t.hT = a.hhi;
+  t.part = a.part;
+  t.status = a.status;
+  t.limit_ns = wait_limit_ns();
+  t.drain_ns = t.limit_ns > 2000000000ull ? t.limit_ns : 2000000000ull;
+  CUtensorMap m128, m32, m8, mx, mw2, mh;
+  const void* w2base = a.packed ? static_cast<const void*>(a.W1) : static_cast<const void*>(a.W2);
+  if (!make_map(&m128, a.W1, w1row, D.n, w1row, 128) || !make_map(&m32, a.W1, w1row, D.n, w1row, 32) ||
+      !make_map(&m8, a.W1, w1row, D.n, w1row, 8) ||
+      !make_map(&mx, a.xhi, D.d, bp2, D.d, (unsigned)bp2) ||
+      !make_map(&mw2, w2base, w2row, D.n, w2row, 64) ||
+      !make_map(&mh, a.hhi, a.hs, bp2, a.hs, (unsigned)bp2))
+    return PI_OK;
+  *used = true;
+  const bool bf = D.dtype == PI_BF16;
+  using F1 = void (*)(const TdArgs, const CUtensorMap, const CUtensorMap, const CUtensorMap,
+                      const CUtensorMap);
+  F1 f1 = bf ? (D.gated ? td_up_kernel<1, true> : td_up_kernel<1, false>)
+             : (D.gated ? td_up_kernel<0, true> : td_up_kernel<0, false>);
+  const int smem1 = t.ns1 * t.stage1 + guard1 + 1024;
+  pi_status s = ensure_smem(reinterpret_cast<const void*>(f1), smem1);
+  if (s != PI_OK) return s;
+  if (launch_chain(f1, P, kTdThreads, smem1, st, t, m128, m32, m8, mx) != cudaSuccess)
+    return PI_ERR_CUDA;
+  using F2 = void (*)(const TdArgs, const CUtensorMap, const CUtensorMap);
+  F2 f2 = bf ? td_down_kernel<1> : td_down_kernel<0>;
+  const int smem2 = t.ns2 * t.stage2 + 1024;
+  s = ensure_smem(reinterpret_cast<const void*>(f2), smem2);
+  if (s != PI_OK) return s;
+  if (launch_chain(f2, P, kTdThreads, smem2, st, t, mw2, mh) != cudaSuccess) return PI_ERR_CUDA;
+  const int g3 = std::max(1, std::min((a.batch * 128 + 255) / 256, (4 * P + nct - 1) / nct));
+  if (launch_chain(td_sum_kernel, nct * g3, 256, 0, st, t) != cudaSuccess) return PI_ERR_CUDA;
+  return PI_OK;
+}
+
 // ------------------------------------------------------------ batched path
 // The three tensor-core phases of a batched sparse FFN over the union of the
 // tokens' active neurons (uidx / ucnt / tmask in device memory).
@@ -415,6 +563,12 @@ pi_status launch_batched(const pi_ffn_desc& D, const pi_layer_weights& w, const 
       launch_chain(bf ? bsplit_x_kernel<1> : bsplit_x_kernel<0>, di.sms * 4, 256, 0, st, a) !=
           cudaSuccess)
     return PI_ERR_CUDA;
+  // the dense FFN on the tensor-memory phases where the shape allows
+  if (a.dense) {
+    bool used = false;
+    s = launch_td(D, a, di, st, &used);
+    if (s != PI_OK || used) return s;
+  }
   // phase 1
   const int nw = D.gated ? 2 : 1;
   // plain layers take 256-column chunks when d allows (fewer pipeline steps

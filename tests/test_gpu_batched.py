@@ -192,3 +192,43 @@ def test_tcgen05_up_projection(gated, monkeypatch):
     for t in tokens:
         want = oracle.dense_ffn(D.L, x[t])
         assert float(np.abs(yd.cpu().numpy()[t] - want).max()) <= Y_TOL * float(np.abs(want).max())
+
+
+def dense_batch(D, x, packed):
+    B = x.shape[0]
+    D.set_packed(packed)
+    try:
+        y = torch.full((B, D.L.d), float("nan"), device=DEV)
+        pi.check(pi.pi_dense_ffn(D.desc, D.w, up(x, DEV), B, y, D.workspace(B)), "pi_dense_ffn")
+        torch.cuda.synchronize()
+    finally:
+        D.set_packed(False)
+    return y.cpu().numpy()
+
+
+@pytest.mark.parametrize("batch,packed", [(2, False), (16, True), (32, False), (32, True)])
+def test_dense_batched_tensor_memory_opt13b(batch, packed):
+    """The dense batched FFN on the tcgen05 / TMA phases, OPT-13B shape:
+    128 or 136 weight rows per block as the MMA's N in phase 1 (x's high and
+    low parts as its M), phase 2's (column tile, neuron block) items split
+    over every block, the blocks' partials summed in block order."""
+    D = opt13b(0.10)
+    x = synth.gen_x(72, batch, batch, 5120)
+    y = dense_batch(D, x, packed)
+    for t in sorted({0, batch // 2, batch - 1}):
+        want = oracle.dense_ffn(D.L, x[t])
+        assert float(np.abs(y[t] - want).max()) <= Y_TOL * float(np.abs(want).max()), t
+
+
+def test_dense_batched_wide_layer():
+    """n = 65536: 432 rows per block, more than one accumulator tile of the
+    tensor-memory phases holds, so the dense FFN takes the mma.sync phases;
+    bit-identical on a second call."""
+    D = dev_layer("wide", lambda: synth.make_layer(1024, 65536, 64, "f16", alpha=0.9,
+                                                    density=0.1, seed=73))
+    x = synth.gen_x(74, 0, 3, 1024)
+    y = dense_batch(D, x, False)
+    for t in range(3):
+        want = oracle.dense_ffn(D.L, x[t])
+        assert float(np.abs(y[t] - want).max()) <= Y_TOL * float(np.abs(want).max()), t
+    np.testing.assert_array_equal(dense_batch(D, x, False), y)
