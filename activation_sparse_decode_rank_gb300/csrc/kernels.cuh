@@ -253,21 +253,28 @@ __device__ void ffn_ring(const FfnArgs& a, const float* xs, const int* lst, cons
     if (lane == 0) {
       // per cold slot: a copy was issued (bit set in `issued`) and the phase
       // parity of the latest one (bit of `par`)
-      unsigned issued = 0u, par = 0u;
+      // entry kc goes to cold slot q = kc % nc in round kc / nc (parity rp),
+      // both advanced by increments: this thread's loop paces the ring
+      unsigned issued = 0u, par = 0u, rp = 0u;
+      int q = 0;
       for (int kc = 0; kc < mc; ++kc) {
-        const int s = nh + kc % nc;
+        // the slot's previous copy (round kc / nc - 1) was released
         // (compute warps that gave up release no slot: this wait then ends
         // at its own bound)
-        if (kc >= nc &&
-            !mbar_wait_sleep(empty + s, (unsigned)((kc / nc - 1) & 1), a.limit_ns)) {
+        if (kc >= nc && !mbar_wait_sleep(empty + nh + q, rp ^ 1u, a.limit_ns)) {
           set_status(a.status, PI_ERR_TIMEOUT);
           *vbad = 1;
           break;
         }
-        if (kc + 1 == a.skip_issue) continue;  // self-test: this slot's phase never completes
-        issue_neuron<GATED>(a, slots, full, s, lst[mh + kc]);
-        issued |= 1u << (s - nh);
-        par = (par & ~(1u << (s - nh))) | ((unsigned)((kc / nc) & 1) << (s - nh));
+        if (kc + 1 != a.skip_issue) {  // self-test: that slot's phase never completes
+          issue_neuron<GATED>(a, slots, full, nh + q, lst[mh + kc]);
+          issued |= 1u << q;
+          par = (par & ~(1u << q)) | (rp << q);
+        }
+        if (++q == nc) {
+          q = 0;
+          rp ^= 1u;
+        }
       }
       // on the normal path the compute warps waited for every copy issued;
       // after a give-up, ring_drain waits for these before the block exits

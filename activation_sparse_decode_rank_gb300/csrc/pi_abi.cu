@@ -79,9 +79,9 @@ WsLayout ws_layout(const pi_ffn_desc& D, int batch) {
     L.xlo = take(2 * (size_t)L.bp * D.d);
     L.hhi = take(2 * (size_t)L.bp * L.hs);
     L.hlo = take(2 * (size_t)L.bp * L.hs);
-    // phase-2 partials: [kGroups2][bp][d] (mma.sync phases) or [P][2][bp][128]
+    // phase-2 partials: [kGroups2][bp][d] (mma.sync phases) or [P][2][bp][256]
     // (tensor-memory phases of the dense FFN)
-    const size_t pg = (size_t)kGroups2 * L.bp * D.d, pt = (size_t)kPMax * 2 * L.bp * 128;
+    const size_t pg = (size_t)kGroups2 * L.bp * D.d, pt = (size_t)kPMax * 2 * L.bp * 256;
     L.bpart = take(sizeof(float) * (pg > pt ? pg : pt));
     L.ppart = take(sizeof(float) * (size_t)kPMax * batch * D.r);  // predictor partials [G][batch][r]
     L.uhi = take(2 * (size_t)L.bp * D.r);
@@ -436,8 +436,9 @@ pi_status launch_td(const pi_ffn_desc& D, const BatchArgs& a, const DevInfo& di,
   const int P = di.sms;
   const int NW = D.gated ? 2 : 1;
   if (D.d % 128 != 0 || D.n % 64 != 0) return PI_OK;
-  const int nct = D.d / 128, nkb = D.n / 64;
-  if (nct > P || (long long)nct * nkb < P) return PI_OK;
+  const int nc2 = D.d % 256 == 0 ? 256 : 128;  // phase 2's columns per tile (the MMA's N)
+  const int nct = D.d / nc2, nkb = D.n / 64;
+  if (nct > P || nct > kTdMaxTiles || P > kPMax || (long long)nct * nkb < P) return PI_OK;
   // the high and low parts of x and of H^T are read as one [2 bp][...] box
   if (a.xlo != a.xhi + (size_t)a.bp * D.d || a.hlo != a.hhi + (size_t)a.bp * a.hs) return PI_OK;
   TdArgs t{};
@@ -457,8 +458,11 @@ pi_status launch_td(const pi_ffn_desc& D, const BatchArgs& a, const DevInfo& di,
   // the last stage's last B read may run (ncol1 - wrows) rows past it
   const int guard1 = (int)round_up((size_t)(t.ncol1 - t.wrows) * 128, 1024);
   t.ns1 = std::min(kTdMaxStages, (budget - guard1) / t.stage1);
-  t.stage2 = (int)round_up((size_t)2 * 64 * 128 + (size_t)bp2 * 128, 1024);
-  t.ns2 = std::min(kTdMaxStages, budget / t.stage2);
+  t.nc2 = nc2;
+  t.stage2 = kTdHalf + (nc2 / 64) * 64 * 128;
+  // batch 32: the low parts' accumulator lanes staged in shared memory
+  const int xst = a.bp == 32 ? (int)round_up((size_t)32 * (nc2 + 4) * sizeof(float), 1024) : 0;
+  t.ns2 = std::min(kTdMaxStages, (budget - xst) / t.stage2);
   if (t.ns1 < 2 || t.ns2 < 2) return PI_OK;
   // the phase-1 epilogue's staging of the accumulators fits in the stages
   if ((size_t)NW * bp2 * (t.ncol1 + 4) * sizeof(float) > (size_t)t.ns1 * t.stage1) return PI_OK;
@@ -468,7 +472,7 @@ pi_status launch_td(const pi_ffn_desc& D, const BatchArgs& a, const DevInfo& di,
     return p;
   };
   t.tcols1 = pow2(NW * t.ncol1);
-  t.tcols2 = pow2(2 * bp2);
+  t.tcols2 = pow2(2 * nc2);
   if (t.tcols1 > 512) return PI_OK;
   t.hs = a.hs;
   t.nct = nct;
@@ -482,6 +486,22 @@ pi_status launch_td(const pi_ffn_desc& D, const BatchArgs& a, const DevInfo& di,
   t.y = a.y;
   t.hT = a.hhi;
   t.part = a.part;
+  // phase 2's partition: block b takes work items [b F / P, (b+1) F / P)
+  {
+    const long long F = (long long)nct * nkb;
+    for (int c = 0; c < nct; ++c) {
+      t.tile_b0[c] = 0xffff;
+      t.tile_b1[c] = 0;
+    }
+    for (int b = 0; b < P; ++b) {
+      const long long s0 = (long long)b * F / P, s1 = (long long)(b + 1) * F / P;
+      t.first_tile[b] = (uint16_t)(s0 / nkb);
+      for (long long c = s0 / nkb; c <= (s1 - 1) / nkb; ++c) {
+        if (t.tile_b0[c] == 0xffff) t.tile_b0[c] = (uint16_t)b;
+        t.tile_b1[c] = (uint16_t)b;
+      }
+    }
+  }
   t.status = a.status;
   t.limit_ns = wait_limit_ns();
   t.drain_ns = t.limit_ns > 2000000000ull ? t.limit_ns : 2000000000ull;
@@ -506,11 +526,11 @@ pi_status launch_td(const pi_ffn_desc& D, const BatchArgs& a, const DevInfo& di,
     return PI_ERR_CUDA;
   using F2 = void (*)(const TdArgs, const CUtensorMap, const CUtensorMap);
   F2 f2 = bf ? td_down_kernel<1> : td_down_kernel<0>;
-  const int smem2 = t.ns2 * t.stage2 + 1024;
+  const int smem2 = t.ns2 * t.stage2 + xst + 1024;
   s = ensure_smem(reinterpret_cast<const void*>(f2), smem2);
   if (s != PI_OK) return s;
   if (launch_chain(f2, P, kTdThreads, smem2, st, t, mw2, mh) != cudaSuccess) return PI_ERR_CUDA;
-  const int g3 = std::max(1, std::min((a.batch * 128 + 255) / 256, (4 * P + nct - 1) / nct));
+  const int g3 = std::max(1, std::min((a.batch * nc2 + 255) / 256, (4 * P + nct - 1) / nct));
   if (launch_chain(td_sum_kernel, nct * g3, 256, 0, st, t) != cudaSuccess) return PI_ERR_CUDA;
   return PI_OK;
 }
@@ -772,14 +792,17 @@ void pi_default_cost_model(pi_cost_model* out) {
   const double fused_fix = 15.4, fused_gbs = 4610.0;
   const double union_fix[PI_COST_TIERS] = {41.3, 41.3, 43.9, 51.6};
   const double union_gbs[PI_COST_TIERS] = {2628.0, 2628.0, 2405.0, 1826.0};
-  const double dense_gbs[PI_COST_TIERS] = {5926.0, 2882.0, 2846.0, 2110.0};
+  // dense: the batch-1 kernel, then the tensor-memory phases (a fixed cost
+  // for the operand split and the partial sum)
+  const double dense_fix[PI_COST_TIERS] = {3.0, 8.0, 8.0, 8.0};
+  const double dense_gbs[PI_COST_TIERS] = {5926.0, 5010.0, 4900.0, 4760.0};
   for (int t = 0; t < PI_COST_TIERS; ++t) {
     out->tier_max_batch[t] = tiers[t];
     out->fixed_us[PI_PATH_FUSED][t] = out->fixed_us[PI_PATH_PER_TOKEN][t] = fused_fix;
     out->gbs[PI_PATH_FUSED][t] = out->gbs[PI_PATH_PER_TOKEN][t] = fused_gbs;
     out->fixed_us[PI_PATH_UNION][t] = union_fix[t];
     out->gbs[PI_PATH_UNION][t] = union_gbs[t];
-    out->fixed_us[PI_PATH_DENSE][t] = 3.0;
+    out->fixed_us[PI_PATH_DENSE][t] = dense_fix[t];
     out->gbs[PI_PATH_DENSE][t] = dense_gbs[t];
   }
 }

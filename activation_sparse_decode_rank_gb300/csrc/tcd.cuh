@@ -34,6 +34,7 @@ namespace pik {
 constexpr int kTdThreads = 192;
 constexpr int kTdMaxStages = 12;
 constexpr int kTdHalf = 128 * 128;  // bytes of one 128-row x 64-column half tile
+constexpr int kTdMaxTiles = 256;    // column tiles of phase 2 (d <= 32768)
 
 struct TdArgs {
   int d, n, batch, bp;
@@ -45,16 +46,20 @@ struct TdArgs {
   int stage1, stage2;  // bytes per stage (multiples of 1024)
   int tcols1, tcols2;  // tensor-memory columns (powers of 2, >= 32)
   int hs;            // row stride of H^T
-  int nct, nkb;      // phase 2: column tiles of 128 (d / 128), neuron blocks of 64 (n / 64)
+  int nct, nkb;      // phase 2: column tiles (d / nc2), neuron blocks of 64 (n / 64)
+  int nc2;           // phase 2: columns per tile (256, or 128 where d % 256 != 0)
   int w2x;           // column of W2 within the W2 tensor's rows (packed records: m1 d)
   const float* b1;
   const float* b2;
   const float* residual;  // [batch][d] or NULL
   float* y;               // [batch][d]
   uint16_t* hT;           // H^T [2 bp][hs]: high parts, then low parts
-  float* part;            // phase 2 partials [P][2][bp][128]
+  float* part;            // phase 2 partials [P][2][bp][nc2]
   int* status;
   unsigned long long limit_ns, drain_ns;
+  // phase 2's partition, from the host: the first and last block with work
+  // items in column tile ct, and each block's first column tile
+  uint16_t tile_b0[kTdMaxTiles], tile_b1[kTdMaxTiles], first_tile[kPMax];
 };
 
 // ---------------------------------------------------------------- helpers
@@ -154,7 +159,7 @@ __device__ __forceinline__ void td_mma_drain(uint64_t* fin, unsigned long long n
 // add high and low parts, bias, activation, and store H^T.
 template <int DT, bool GATED>
 __global__ void __launch_bounds__(kTdThreads, 1)
-    td_up_kernel(const TdArgs a, const __grid_constant__ CUtensorMap mw128,
+    td_up_kernel(const __grid_constant__ TdArgs a, const __grid_constant__ CUtensorMap mw128,
                  const __grid_constant__ CUtensorMap mw32, const __grid_constant__ CUtensorMap mw8,
                  const __grid_constant__ CUtensorMap mx) {
   pdl_enter();
@@ -306,24 +311,31 @@ __global__ void __launch_bounds__(kTdThreads, 1)
 }
 
 // ---------------------------------------------------------------- phase 2
-// Work items f = ct nkb + kb (column tile ct of 128 outputs, neuron block kb
-// of 64) split evenly over the blocks: block b takes [b F / P, (b+1) F / P)
-// and, as nct <= P, touches at most two column tiles (segments 0 and 1,
-// accumulated in tensor-memory columns [seg 2bp, seg 2bp + 2bp)).  Stage
-// layout: W2 halves (columns ct 128 + [0, 64) and [64, 128)) of 64 neuron
-// rows (8 KB each), then H^T's box [2 bp][64 neurons].
+// Work items f = ct nkb + kb (column tile ct of nc2 = 256 or 128 outputs,
+// block kb of 64 neurons) split evenly over the blocks: block b takes
+// [b F / P, (b+1) F / P) and, as nct <= P, touches at most two column tiles
+// (segments 0 and 1, accumulated in tensor-memory columns [seg nc2, seg nc2
+// + nc2)).  D[j][c] = sum_i H2[j][i] W2[i][ct nc2 + c]: A = H^T's high and
+// low parts (M = 128 rows, the first 2 bp loaded), B = the tile's columns
+// of the block's W2 rows, N-major (nc2 / 64 boxes of 64 columns x 64 rows,
+// lbo the distance of the boxes), one chain of four MMAs per item.  Stage
+// layout: H^T's box region (16 KB), then the W2 boxes (8 KB each).
+// Epilogue per segment: accumulator lanes t < bp hold the high parts' sums
+// and bp + t the low parts' (batch <= 16: one warp, added by shuffle;
+// batch 32: the low lanes' warp stages them in shared memory); the block
+// writes its partial of the column tile.
 __device__ __forceinline__ long long td_start(int b, long long F, int P) { return (long long)b * F / P; }
 
 template <int DT>
 __global__ void __launch_bounds__(kTdThreads, 1)
-    td_down_kernel(const TdArgs a, const __grid_constant__ CUtensorMap mw2,
+    td_down_kernel(const __grid_constant__ TdArgs a, const __grid_constant__ CUtensorMap mw2,
                    const __grid_constant__ CUtensorMap mh) {
   pdl_enter();
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char* sm = align1024(smraw);
   __shared__ __align__(8) uint64_t full[kTdMaxStages], empty[kTdMaxStages], accf[2], fin;
   __shared__ uint32_t s_taddr;
-  __shared__ int s_bad, s_it;
+  __shared__ int s_bad, s_it, s_efail;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const long long F = (long long)a.nct * a.nkb;
   const int f0 = (int)td_start(blockIdx.x, F, a.P), f1 = (int)td_start(blockIdx.x + 1, F, a.P);
@@ -331,7 +343,10 @@ __global__ void __launch_bounds__(kTdThreads, 1)
   const int nseg = (f1 > f0) ? ((f1 - 1) / a.nkb - ct0 + 1) : 0;  // 1 or 2
   const int ns = a.ns2;
   const int bp2 = 2 * a.bp;
-  constexpr int kW2Half = 64 * 128;  // 64 neuron rows x 64 columns
+  const int nc2 = a.nc2, nbox = a.nc2 >> 6;
+  constexpr int kW2Box = 64 * 128;  // 64 neuron rows x 64 columns
+  float* X = reinterpret_cast<float*>(sm + (size_t)ns * a.stage2);  // [32][nc2 + 4] (batch 32)
+  const int xp = nc2 + 4;
 
   if (warp == 1) tmem_alloc(&s_taddr, (uint32_t)a.tcols2);
   if (tid == 0) {
@@ -345,6 +360,7 @@ __global__ void __launch_bounds__(kTdThreads, 1)
     fence_mbar_init();
     s_bad = 0;
     s_it = 0;
+    s_efail = 0;
   }
   tc_fence_before();
   __syncthreads();
@@ -355,7 +371,7 @@ __global__ void __launch_bounds__(kTdThreads, 1)
   if (warp == 0) {
     if (lane == 0) {  // TMA producer
       const uint64_t pw = l2_evict_first(), ph = l2_evict_last();
-      const unsigned tx = (unsigned)(2 * kW2Half + bp2 * 128);
+      const unsigned tx = (unsigned)(nbox * kW2Box + bp2 * 128);
       int it = 0;
       for (int f = f0; f < f1; ++f, ++it) {
         const int s = it % ns;
@@ -367,15 +383,16 @@ __global__ void __launch_bounds__(kTdThreads, 1)
         const int ct = f / a.nkb, kb = f - ct * a.nkb;
         unsigned char* st = sm + (size_t)s * a.stage2;
         mbar_expect_tx(full + s, tx);
-        tma2d(st, &mw2, a.w2x + ct * 128, kb * 64, full + s, pw);
-        tma2d(st + kW2Half, &mw2, a.w2x + ct * 128 + 64, kb * 64, full + s, pw);
-        tma2d(st + 2 * kW2Half, &mh, kb * 64, 0, full + s, ph);
+        tma2d(st, &mh, kb * 64, 0, full + s, ph);
+        for (int g = 0; g < nbox; ++g)
+          tma2d(st + kTdHalf + g * kW2Box, &mw2, a.w2x + ct * nc2 + 64 * g, kb * 64, full + s, pw);
       }
       s_it = it;
     }
   } else if (warp == 1) {
     if (lane == 0) {  // MMA issuer
-      const uint32_t idesc = td_idesc(DT, bp2, true);
+      // A K-major, B N-major (transposed), M = 128, N = nc2
+      const uint32_t idesc = td_idesc(DT, nc2, false) | (1u << 16);
       int it = 0;
       for (int f = f0; f < f1; ++f, ++it) {
         const int s = it % ns;
@@ -390,36 +407,76 @@ __global__ void __launch_bounds__(kTdThreads, 1)
         const bool first = (f == f0) || (f == ct * a.nkb);
         const uint32_t sa = smem_u32(sm + (size_t)s * a.stage2);
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t adesc = sw128_desc(sa + 2048u * ks, (uint32_t)kW2Half, 1024u);
-          const uint64_t bdesc = sw128_desc(sa + (uint32_t)(2 * kW2Half) + 32u * ks, 16u, 1024u);
-          tc_mma(taddr + (uint32_t)(seg * bp2), adesc, bdesc, idesc, (!first || ks > 0) ? 1u : 0u);
-        }
+        for (int ks = 0; ks < 4; ++ks)
+          tc_mma(taddr + (uint32_t)(seg * nc2), sw128_desc(sa + 32u * ks, 16u, 1024u),
+                 sw128_desc(sa + (uint32_t)kTdHalf + 2048u * ks, (uint32_t)kW2Box, 1024u), idesc,
+                 (!first || ks > 0) ? 1u : 0u);
         tc_commit(empty + s);
         if (f + 1 == f1 || (f + 1) % a.nkb == 0) tc_commit(accf + seg);  // segment complete
       }
     }
-  } else {  // epilogue: lanes = output columns of the tile
+  } else {  // epilogue: warps 2..5; accumulator lanes 0..63 are warps 4 and 5's
     const int q = warp & 3;
     const uint32_t lanebase = taddr + ((uint32_t)(q * 32) << 16);
     for (int seg = 0; seg < nseg; ++seg) {
       if (!mbar_wait(accf + seg, 0u, a.limit_ns)) {
         set_status(a.status, PI_ERR_TIMEOUT);
         *vbad = 1;
-        break;
+        s_efail = 1;  // written by epilogue threads only, before the barrier
       }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (s_efail) break;  // uniform over the four epilogue warps
       tc_fence_after();
-      float* dst = a.part + (((size_t)blockIdx.x * 2 + seg) * a.bp) * 128 + q * 32 + lane;
-      for (int t0 = 0; t0 < a.bp; t0 += 8) {
-        uint32_t hi[8], lo[8];
-        td_ld8(hi, lanebase + (uint32_t)(seg * bp2 + t0));
-        td_ld8(lo, lanebase + (uint32_t)(seg * bp2 + a.bp + t0));
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      const uint32_t col0 = (uint32_t)(seg * nc2);
+      float* prow = a.part + ((size_t)blockIdx.x * 2 + seg) * a.bp * nc2;  // [bp][nc2]
+      if (a.bp == 16) {
+        if (q == 0) {  // lanes 0..15: high parts, 16..31: low parts
+          for (int c0 = 0; c0 < nc2; c0 += 8) {
+            uint32_t v[8];
+            td_ld8(v, lanebase + col0 + (uint32_t)c0);
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            float o[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          if (t0 + e < a.batch)
-            __stcg(dst + (size_t)(t0 + e) * 128, __uint_as_float(hi[e]) + __uint_as_float(lo[e]));
+            for (int e = 0; e < 8; ++e)
+              o[e] = __uint_as_float(v[e]) + __shfl_down_sync(0xffffffffu, __uint_as_float(v[e]), 16);
+            if (lane < a.batch) {
+              float4* dst = reinterpret_cast<float4*>(prow + (size_t)lane * nc2 + c0);
+              __stcg(dst, make_float4(o[0], o[1], o[2], o[3]));
+              __stcg(dst + 1, make_float4(o[4], o[5], o[6], o[7]));
+            }
+          }
+        }
+      } else {  // bp == 32: warp 5 (lanes 32..63, low parts) stages, warp 4 adds
+        if (q == 1) {
+          for (int c0 = 0; c0 < nc2; c0 += 8) {
+            uint32_t v[8];
+            td_ld8(v, lanebase + col0 + (uint32_t)c0);
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            float* xr = X + (size_t)lane * xp + c0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xr[e] = __uint_as_float(v[e]);
+          }
+        }
+        if (q < 2) asm volatile("bar.sync 2, 64;" ::: "memory");  // warps 4 and 5 only
+        if (q == 0) {
+          for (int c0 = 0; c0 < nc2; c0 += 8) {
+            uint32_t v[8];
+            td_ld8(v, lanebase + col0 + (uint32_t)c0);
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            const float* xr = X + (size_t)lane * xp + c0;
+            float o[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = __uint_as_float(v[e]) + xr[e];
+            if (lane < a.batch) {
+              float4* dst = reinterpret_cast<float4*>(prow + (size_t)lane * nc2 + c0);
+              __stcg(dst, make_float4(o[0], o[1], o[2], o[3]));
+              __stcg(dst + 1, make_float4(o[4], o[5], o[6], o[7]));
+            }
+          }
+        }
       }
+      // X is read by warp 4 before warp 5 stages the next segment
+      asm volatile("bar.sync 1, 128;" ::: "memory");
     }
   }
   tc_fence_before();
@@ -436,39 +493,20 @@ __global__ void __launch_bounds__(kTdThreads, 1)
 }
 
 // ---------------------------------------------------------------- phase 3
-// y[t][c] = b2[c] + sum over the blocks whose work items touch column tile
-// c / 128, in block order, of their partials (+ residual).  Block j of the
-// grid takes column tile j % nct and outputs (t, column) of the tile from
-// j / nct on; thread 0 lists the tile's blocks and their segments first.
-__global__ void __launch_bounds__(256) td_sum_kernel(const TdArgs a) {
+// y[t][c] = b2[c] + the partials of the blocks with work items in column
+// tile ct = c / nc2, in block order (the host's table), + residual.  Block j
+// takes tile j % nct and its outputs e = (j / nct) 256 + thread, ...
+__global__ void __launch_bounds__(256) td_sum_kernel(const __grid_constant__ TdArgs a) {
   pdl_enter();
-  __shared__ int s_b[kPMax + 2], s_seg[kPMax + 2], s_nb;
   const int ct = blockIdx.x % a.nct, g = blockIdx.x / a.nct, ng = gridDim.x / a.nct;
-  if (threadIdx.x == 0) {
-    const long long F = (long long)a.nct * a.nkb;
-    const long long fs = (long long)ct * a.nkb, fe = fs + a.nkb - 1;
-    // the block whose range holds fs: the largest b with start(b) <= fs
-    int b = (int)(fs * a.P / F);
-    while (b + 1 < a.P && td_start(b + 1, F, a.P) <= fs) ++b;
-    while (b > 0 && td_start(b, F, a.P) > fs) --b;
-    int nb = 0;
-    for (; b < a.P && td_start(b, F, a.P) <= fe; ++b) {
-      const long long sb = td_start(b, F, a.P), eb = td_start(b + 1, F, a.P);
-      if (eb <= sb) continue;  // no work items
-      s_b[nb] = b;
-      s_seg[nb] = (int)(ct - sb / a.nkb);
-      ++nb;
-    }
-    s_nb = nb;
-  }
-  __syncthreads();
-  const int nb = s_nb;
-  for (int e = g * 256 + (int)threadIdx.x; e < a.batch * 128; e += ng * 256) {
-    const int t = e >> 7, cl = e & 127;
+  const int b0 = a.tile_b0[ct], b1 = a.tile_b1[ct];
+  const int nc2 = a.nc2, tot = a.batch * nc2;
+  for (int e = g * 256 + (int)threadIdx.x; e < tot; e += ng * 256) {
+    const int t = e / nc2, cl = e - t * nc2;
     float s = 0.f;
-    for (int k = 0; k < nb; ++k)
-      s += __ldcg(a.part + (((size_t)s_b[k] * 2 + s_seg[k]) * a.bp + t) * 128 + cl);
-    const int c = ct * 128 + cl;
+    for (int b = b0; b <= b1; ++b)
+      s += __ldcg(a.part + (((size_t)b * 2 + (ct - a.first_tile[b])) * a.bp + t) * nc2 + cl);
+    const int c = ct * nc2 + cl;
     if (a.b2) s += a.b2[c];
     const size_t o = (size_t)t * a.d + c;
     if (a.residual) s += a.residual[o];
