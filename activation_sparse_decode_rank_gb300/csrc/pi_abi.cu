@@ -441,6 +441,9 @@ pi_status launch_td(const pi_ffn_desc& D, const BatchArgs& a, const DevInfo& di,
   if (nct > P || nct > kTdMaxTiles || P > kPMax || (long long)nct * nkb < P) return PI_OK;
   // the high and low parts of x and of H^T are read as one [2 bp][...] box
   if (a.xlo != a.xhi + (size_t)a.bp * D.d || a.hlo != a.hhi + (size_t)a.bp * a.hs) return PI_OK;
+  // the final sum moves four columns at a time (y, b2 and the weights are
+  // checked for 16-byte alignment at the entry points)
+  if (a.residual && !aligned16(a.residual)) return PI_OK;
   TdArgs t{};
   t.d = D.d;
   t.n = D.n;
@@ -530,7 +533,7 @@ pi_status launch_td(const pi_ffn_desc& D, const BatchArgs& a, const DevInfo& di,
   s = ensure_smem(reinterpret_cast<const void*>(f2), smem2);
   if (s != PI_OK) return s;
   if (launch_chain(f2, P, kTdThreads, smem2, st, t, mw2, mh) != cudaSuccess) return PI_ERR_CUDA;
-  const int g3 = std::max(1, std::min((a.batch * nc2 + 255) / 256, (4 * P + nct - 1) / nct));
+  const int g3 = std::max(1, std::min((a.batch * nc2 / 4 + 255) / 256, (4 * P + nct - 1) / nct));
   if (launch_chain(td_sum_kernel, nct * g3, 256, 0, st, t) != cudaSuccess) return PI_ERR_CUDA;
   return PI_OK;
 }
@@ -795,7 +798,7 @@ void pi_default_cost_model(pi_cost_model* out) {
   // dense: the batch-1 kernel, then the tensor-memory phases (a fixed cost
   // for the operand split and the partial sum)
   const double dense_fix[PI_COST_TIERS] = {3.0, 8.0, 8.0, 8.0};
-  const double dense_gbs[PI_COST_TIERS] = {5926.0, 5010.0, 4900.0, 4760.0};
+  const double dense_gbs[PI_COST_TIERS] = {5926.0, 5910.0, 5780.0, 5300.0};
   for (int t = 0; t < PI_COST_TIERS; ++t) {
     out->tier_max_batch[t] = tiers[t];
     out->fixed_us[PI_PATH_FUSED][t] = out->fixed_us[PI_PATH_PER_TOKEN][t] = fused_fix;

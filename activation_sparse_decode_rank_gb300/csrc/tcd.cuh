@@ -500,17 +500,36 @@ __global__ void __launch_bounds__(256) td_sum_kernel(const __grid_constant__ TdA
   pdl_enter();
   const int ct = blockIdx.x % a.nct, g = blockIdx.x / a.nct, ng = gridDim.x / a.nct;
   const int b0 = a.tile_b0[ct], b1 = a.tile_b1[ct];
-  const int nc2 = a.nc2, tot = a.batch * nc2;
+  const int nc2 = a.nc2, q4 = nc2 >> 2, tot = a.batch * q4;  // four columns per thread
   for (int e = g * 256 + (int)threadIdx.x; e < tot; e += ng * 256) {
-    const int t = e / nc2, cl = e - t * nc2;
-    float s = 0.f;
-    for (int b = b0; b <= b1; ++b)
-      s += __ldcg(a.part + (((size_t)b * 2 + (ct - a.first_tile[b])) * a.bp + t) * nc2 + cl);
+    const int t = e / q4, cl = 4 * (e - t * q4);
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int b = b0; b <= b1; ++b) {  // (unrolled: the partials' loads go out together)
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(
+          a.part + (((size_t)b * 2 + (ct - a.first_tile[b])) * a.bp + t) * nc2 + cl));
+      s.x += v.x;
+      s.y += v.y;
+      s.z += v.z;
+      s.w += v.w;
+    }
     const int c = ct * nc2 + cl;
-    if (a.b2) s += a.b2[c];
+    if (a.b2) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(a.b2 + c));
+      s.x += v.x;
+      s.y += v.y;
+      s.z += v.z;
+      s.w += v.w;
+    }
     const size_t o = (size_t)t * a.d + c;
-    if (a.residual) s += a.residual[o];
-    a.y[o] = s;
+    if (a.residual) {
+      const float4 v = *reinterpret_cast<const float4*>(a.residual + o);
+      s.x += v.x;
+      s.y += v.y;
+      s.z += v.z;
+      s.w += v.w;
+    }
+    *reinterpret_cast<float4*>(a.y + o) = s;
   }
 }
 
