@@ -232,3 +232,31 @@ def test_dense_batched_wide_layer():
         want = oracle.dense_ffn(D.L, x[t])
         assert float(np.abs(y[t] - want).max()) <= Y_TOL * float(np.abs(want).max()), t
     np.testing.assert_array_equal(dense_batch(D, x, False), y)
+
+
+@pytest.mark.parametrize("batch", [8, 24])
+def test_dense_batched_tensor_memory_128_column_tiles(batch):
+    """d = 1152 (a multiple of 128, not of 256): phase 2 takes 128-column
+    tiles; 16 and 32 padded tokens (the one-warp and the two-warp
+    epilogue); n = 4096: 32 rows per block in phase 1."""
+    D = dev_layer("d1152", lambda: synth.make_layer(1152, 4096, 64, "f16", alpha=0.9,
+                                                     density=0.1, seed=75))
+    x = synth.gen_x(76, batch, batch, 1152)
+    for packed in (False, True):
+        y = dense_batch(D, x, packed)
+        for t in sorted({0, batch - 1}):
+            want = oracle.dense_ffn(D.L, x[t])
+            assert float(np.abs(y[t] - want).max()) <= Y_TOL * float(np.abs(want).max()), (packed, t)
+
+
+def test_dense_batched_tensor_memory_gated_batch32():
+    """Gated bf16 Llama-2-7B shape at batch 32: two weight tiles (gate, up)
+    per stage in phase 1, 256-column tiles and the two-warp epilogue in
+    phase 2."""
+    D = dev_layer("llama", lambda: synth.make_layer(4096, 11008, 256, "bf16", gated=True,
+                                                     alpha=1.0, density=0.10, seed=3))
+    x = synth.gen_x(77, 0, 32, 4096)
+    y = dense_batch(D, x, True)
+    for t in (0, 13, 31):
+        want = oracle.dense_ffn(D.L, x[t])
+        assert float(np.abs(y[t] - want).max()) <= Y_TOL * float(np.abs(want).max()), t
