@@ -123,11 +123,19 @@ template <int DT, int TB>
 __global__ void __launch_bounds__(256) bpu_partial_kernel(const uint16_t* Bm, const float* x, int d,
                                                           int r, int batch, int G, float* part,
                                                           uint16_t* xhi, uint16_t* xlo, int bp) {
-  pdl_enter();
   extern __shared__ __align__(16) float xs[];  // [batch][w]
   const int c = blockIdx.x, tid = threadIdx.x, nch = d >> 3;
   const int q0 = (int)((long long)c * nch / G), q1 = (int)((long long)(c + 1) * nch / G);
   const int nq = q1 - q0, w = nq * 8;
+  // the block's columns of Bm (weights, not written by the kernels before
+  // this one) head for L2 while those finish; x after the wait
+  for (int k = tid; k < r; k += 256) {
+    const char* p0 = reinterpret_cast<const char*>(Bm + (size_t)k * d + 8 * q0);
+    const char* p1 = p0 + 16 * nq;  // every address prefetched lies in [p0, p1)
+    for (const char* p = p0; p < p1; p += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+    if (nq > 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(p1 - 16));
+  }
+  pdl_enter();
   for (int e = tid; e < batch * w; e += 256) {
     const int t = e / w, j = e - t * w;
     xs[e] = x[(size_t)t * d + 8 * q0 + j];
@@ -205,7 +213,6 @@ template <int DT, int MT>
 __global__ void __launch_bounds__(256) blogit_kernel(const uint16_t* A, const float* b1,
                                                      const uint16_t* uhi, const uint16_t* ulo, int n,
                                                      int r, int batch, int bp, float* logits) {
-  pdl_enter();
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rowb = 2 * r + 16;
@@ -214,12 +221,15 @@ __global__ void __launch_bounds__(256) blogit_kernel(const uint16_t* A, const fl
   const int i0 = blockIdx.x * kLT;
   const int tn = min(kLT, n - i0);
   const int pcs = r >> 3;
+  // the A rows (weights, not written by the kernels before this one) load
+  // while those finish; u after the wait
   for (int e = tid; e < kLT * pcs; e += 256) {
     const int row = e / pcs, pc = e - row * pcs;
     unsigned char* dst = As + (size_t)row * rowb + 16 * pc;
     if (row < tn) cp_async16(dst, A + (size_t)(i0 + row) * r + 8 * pc);
     else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
   }
+  pdl_enter();
   for (int e = tid; e < 2 * bp * pcs; e += 256) {
     const int rw = e / pcs, pc = e - rw * pcs;
     const int prt = rw / bp, t = rw - prt * bp;

@@ -162,7 +162,6 @@ __global__ void __launch_bounds__(kTdThreads, 1)
     td_up_kernel(const __grid_constant__ TdArgs a, const __grid_constant__ CUtensorMap mw128,
                  const __grid_constant__ CUtensorMap mw32, const __grid_constant__ CUtensorMap mw8,
                  const __grid_constant__ CUtensorMap mx) {
-  pdl_enter();
   constexpr int NW = GATED ? 2 : 1;
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char* sm = align1024(smraw);
@@ -198,12 +197,39 @@ __global__ void __launch_bounds__(kTdThreads, 1)
   const uint32_t taddr = s_taddr;
   volatile int* vbad = &s_bad;
 
+  // the weight boxes of the first stages: the weights are not written by
+  // the kernels before this one, so they load while those finish
+  const uint64_t pw = l2_evict_first(), px = l2_evict_last();
+  const unsigned tx = (unsigned)(NW * rows * 128 + bp2 * 128);
+  auto issue_w = [&](int it, int s) {
+    unsigned char* st = sm + (size_t)s * a.stage1;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      unsigned char* wt = st + kTdHalf + (size_t)w * a.wrows * 128;
+      const int xc = w * a.d + it * 64;
+      int r = 0;
+      while (r < rows) {
+        const int rem = rows - r;
+        const CUtensorMap* m = rem >= 128 ? &mw128 : (rem >= 32 ? &mw32 : &mw8);
+        const int h = rem >= 128 ? 128 : (rem >= 32 ? 32 : 8);
+        tma2d(wt + (size_t)r * 128, m, xc, row0 + r, full + s, pw);
+        r += h;
+      }
+    }
+  };
+  const int npre = rows > 0 ? min(ns, nkb) : 0;
+  if (tid == 0)
+    for (int it = 0; it < npre; ++it) {
+      mbar_expect_tx(full + it, tx);  // the stage's x box comes after the wait below
+      issue_w(it, it);
+    }
+  pdl_enter();  // the previous kernel's results (x's high / low parts) are visible from here
+
   if (rows > 0) {
     if (warp == 0) {
       if (lane == 0) {  // TMA producer
-        const uint64_t pw = l2_evict_first(), px = l2_evict_last();
-        const unsigned tx = (unsigned)(NW * rows * 128 + bp2 * 128);
-        int it = 0;
+        for (int it = 0; it < npre; ++it) tma2d(sm + (size_t)it * a.stage1, &mx, it * 64, 0, full + it, px);
+        int it = npre;
         for (; it < nkb; ++it) {
           const int s = it % ns;
           if (it >= ns &&
@@ -215,19 +241,7 @@ __global__ void __launch_bounds__(kTdThreads, 1)
           unsigned char* st = sm + (size_t)s * a.stage1;
           mbar_expect_tx(full + s, tx);
           tma2d(st, &mx, it * 64, 0, full + s, px);
-#pragma unroll
-          for (int w = 0; w < NW; ++w) {
-            unsigned char* wt = st + kTdHalf + (size_t)w * a.wrows * 128;
-            const int xc = w * a.d + it * 64;
-            int r = 0;
-            while (r < rows) {
-              const int rem = rows - r;
-              const CUtensorMap* m = rem >= 128 ? &mw128 : (rem >= 32 ? &mw32 : &mw8);
-              const int h = rem >= 128 ? 128 : (rem >= 32 ? 32 : 8);
-              tma2d(wt + (size_t)r * 128, m, xc, row0 + r, full + s, pw);
-              r += h;
-            }
-          }
+          issue_w(it, s);
         }
         s_it = it;
       }
@@ -330,7 +344,6 @@ template <int DT>
 __global__ void __launch_bounds__(kTdThreads, 1)
     td_down_kernel(const __grid_constant__ TdArgs a, const __grid_constant__ CUtensorMap mw2,
                    const __grid_constant__ CUtensorMap mh) {
-  pdl_enter();
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char* sm = align1024(smraw);
   __shared__ __align__(8) uint64_t full[kTdMaxStages], empty[kTdMaxStages], accf[2], fin;
@@ -368,12 +381,29 @@ __global__ void __launch_bounds__(kTdThreads, 1)
   const uint32_t taddr = s_taddr;
   volatile int* vbad = &s_bad;
 
+  // the W2 boxes of the first items: the weights are not written by the
+  // kernels before this one, so they load while those finish
+  const uint64_t pw = l2_evict_first(), ph = l2_evict_last();
+  const unsigned tx = (unsigned)(nbox * kW2Box + bp2 * 128);
+  const int npre = min(ns, f1 - f0);
+  if (tid == 0)
+    for (int it = 0; it < npre; ++it) {
+      const int f = f0 + it, ct = f / a.nkb, kb = f - ct * a.nkb;
+      unsigned char* st = sm + (size_t)it * a.stage2;
+      mbar_expect_tx(full + it, tx);  // the item's H^T box comes after the wait below
+      for (int g = 0; g < nbox; ++g)
+        tma2d(st + kTdHalf + g * kW2Box, &mw2, a.w2x + ct * nc2 + 64 * g, kb * 64, full + it, pw);
+    }
+  pdl_enter();  // phase 1's H^T is visible from here
+
   if (warp == 0) {
     if (lane == 0) {  // TMA producer
-      const uint64_t pw = l2_evict_first(), ph = l2_evict_last();
-      const unsigned tx = (unsigned)(nbox * kW2Box + bp2 * 128);
-      int it = 0;
-      for (int f = f0; f < f1; ++f, ++it) {
+      for (int it = 0; it < npre; ++it) {
+        const int f = f0 + it, kb = f - (f / a.nkb) * a.nkb;
+        tma2d(sm + (size_t)it * a.stage2, &mh, kb * 64, 0, full + it, ph);
+      }
+      int it = npre;
+      for (int f = f0 + npre; f < f1; ++f, ++it) {
         const int s = it % ns;
         if (it >= ns && !mbar_wait_sleep(empty + s, (unsigned)(((it / ns) - 1) & 1), a.limit_ns)) {
           set_status(a.status, PI_ERR_TIMEOUT);
