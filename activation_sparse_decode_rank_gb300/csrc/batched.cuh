@@ -313,19 +313,25 @@ __global__ void __launch_bounds__(512, 1) bup_kernel(const BatchArgs a) {
   const int hi_u = (int)((long long)(blockIdx.x + 1) * U / a.P);
   const int stage_bytes = bup_stage_bytes<GATED, BK>(a.bp);
   constexpr int NW = GATED ? 2 : 1;
-  // warp -> (n group: n tiles 2 ng and 2 ng + 1; k quarter: k-steps
-  // kq, kq + 4, ...), every m tile: one x fragment feeds 2 NW products per
-  // part, the B fragments of both n tiles come in one ldmatrix.x4
-  const int ng = warp & 3, kq = warp >> 2;
   const int ksteps = BK / 16;
   const int nchunks = a.d / BK;
   constexpr int S = kBStages;
   constexpr int CV = NW * MT * 2 * 4;  // accumulator values per lane
-  float* comb = reinterpret_cast<float*>(smem + S * stage_bytes);  // [3][4][32][CV]
+  // the k slices' partial sums [KQ - 1][NG][32][CV], in the stages (free
+  // between a tile's last chunk and the next tile's first copies)
+  float* comb = reinterpret_cast<float*>(smem);
   const size_t w1s = a.packed ? (size_t)a.rec : (GATED ? 2 * (size_t)a.d : (size_t)a.d);
 
   for (int t0 = lo_u; t0 < hi_u; t0 += kBT) {
     const int tn = min(kBT, hi_u - t0);
+    // warp -> (n group ng of 16 rows: n tiles 2 ng and 2 ng + 1; k slice
+    // kq: k-steps kq, kq + KQ, ...): NG groups cover the tile's rows, so a
+    // tile with few rows (a sparse union) spreads its K over more warps;
+    // every m tile: one x fragment feeds 2 NW products per part, the B
+    // fragments of both n tiles come in one ldmatrix.x4
+    const int lg = tn <= 16 ? 0 : (tn <= 32 ? 1 : 2);
+    const int NG = 1 << lg, KQ = 16 >> lg;
+    const int ng = warp & (NG - 1), kq = warp >> lg;
     // issue the cp.async loads of chunk ch into stage ch % S
     auto issue = [&](int ch) {
       unsigned char* st = smem + (ch % S) * stage_bytes;
@@ -371,7 +377,7 @@ __global__ void __launch_bounds__(512, 1) bup_kernel(const BatchArgs a) {
       __syncthreads();
       const unsigned char* st = smem + (ch % S) * stage_bytes;
       const unsigned char* xs_ = st + (size_t)NW * kBT * kRowB;
-      for (int ks = kq; ks < ksteps; ks += 4) {
+      for (int ks = kq; ks < ksteps; ks += KQ) {
         uint32_t ah[MT][4], al[MT][4];
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
@@ -401,7 +407,7 @@ __global__ void __launch_bounds__(512, 1) bup_kernel(const BatchArgs a) {
       }
       __syncthreads();
     }
-    // high + low, then the four k quarters meet in a fixed order (0, 1, 2, 3)
+    // high + low, then the KQ k slices meet in a fixed order (0, 1, ...)
     float v[CV];
 #pragma unroll
     for (int w = 0; w < NW; ++w)
@@ -413,14 +419,14 @@ __global__ void __launch_bounds__(512, 1) bup_kernel(const BatchArgs a) {
           for (int e = 0; e < 4; ++e)
             v[((w * MT + m) * 2 + jn) * 4 + e] = acc[w][m][jn][e] + accl[w][m][jn][e];
     if (kq > 0) {
-      float* cp = comb + ((size_t)((kq - 1) * 4 + ng) * 32 + lane) * CV;
+      float* cp = comb + ((size_t)((kq - 1) * NG + ng) * 32 + lane) * CV;
 #pragma unroll
       for (int e = 0; e < CV; ++e) cp[e] = v[e];
     }
     __syncthreads();
     if (kq == 0) {
-      for (int q = 1; q < 4; ++q) {
-        const float* cp = comb + ((size_t)((q - 1) * 4 + ng) * 32 + lane) * CV;
+      for (int q = 1; q < KQ; ++q) {
+        const float* cp = comb + ((size_t)((q - 1) * NG + ng) * 32 + lane) * CV;
 #pragma unroll
         for (int e = 0; e < CV; ++e) v[e] += cp[e];
       }

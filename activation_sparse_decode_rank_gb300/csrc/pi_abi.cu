@@ -598,8 +598,9 @@ pi_status launch_batched(const pi_ffn_desc& D, const pi_layer_weights& w, const 
   // per byte); gated ones 128 (their stages would not fit three deep)
   const bool wide = !D.gated && D.d % 256 == 0;
   const int rowb = (wide ? 256 : 128) * 2 + 16;
-  const int comb1 = 3 * 4 * 32 * (nw * (m2 ? 2 : 1) * 8) * (int)sizeof(float);  // k-quarter sums
-  const int smem1 = kBStages * ((nw * kBT + 2 * a.bp) * rowb) + comb1;
+  // (the k slices' partial sums reuse the stages: 15 x 32 x CV floats at
+  // most, less than the three stages hold)
+  const int smem1 = kBStages * ((nw * kBT + 2 * a.bp) * rowb);
   using Fn = void (*)(const BatchArgs);
   Fn f1;
   if (!bf) {
