@@ -794,8 +794,8 @@ void pi_default_cost_model(pi_cost_model* out) {
   // per tier (batch <= 1, 4, 16, 32): fixed microseconds and GB/s of a
   // least-squares fit to the measured sweep (five densities per batch)
   const double fused_fix = 15.4, fused_gbs = 4610.0;
-  const double union_fix[PI_COST_TIERS] = {41.3, 41.3, 43.9, 51.6};
-  const double union_gbs[PI_COST_TIERS] = {2628.0, 2628.0, 2405.0, 1826.0};
+  const double union_fix[PI_COST_TIERS] = {34.2, 34.2, 37.9, 51.5};
+  const double union_gbs[PI_COST_TIERS] = {2574.0, 2574.0, 2424.0, 1912.0};
   // dense: the batch-1 kernel, then the tensor-memory phases (a fixed cost
   // for the operand split and the partial sum)
   const double dense_fix[PI_COST_TIERS] = {3.0, 8.0, 8.0, 8.0};

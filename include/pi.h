@@ -357,9 +357,9 @@ typedef struct {
 
 /* The built-in model: fitted on one GB300 (measured copy peak 6.78 TB/s) to
  * the density x batch sweep of the OPT-13B-shaped layer (d 5120, n 20480,
- * r 192, fp16; within 7.8 % of every measured point, the faster path picked
- * at 19 of 20 points, the other a near tie).  Other shapes move the fixed
- * costs (grid-wide waits, launches) by some microseconds. */
+ * r 192, fp16; within 5.8 % of every measured point, the faster path picked
+ * at all 20 points).  Other shapes move the fixed costs (grid-wide waits,
+ * launches) by some microseconds. */
 void pi_default_cost_model(pi_cost_model* out);
 
 /* Fills *out for one layer shape and batch (1..32).  model NULL: the
