@@ -428,7 +428,9 @@ bool batch_legacy() {
 // The dense batched FFN (all n neurons, every token) on the tcgen05 / TMA
 // phases of tcd.cuh, x already split into its high / low parts.  Sets *used
 // = false, launching nothing, where the shape does not fit them (d % 128,
-// n % 64, more column tiles than blocks) or PI_BATCH_LEGACY is set.
+// n % 64, more column tiles than blocks, more than 256 rows per block, a
+// residual that is not 16-byte aligned) or PI_BATCH_LEGACY is set; the
+// mma.sync phases run then.
 pi_status launch_td(const pi_ffn_desc& D, const BatchArgs& a, const DevInfo& di, cudaStream_t st,
                     bool* used) {
   *used = false;

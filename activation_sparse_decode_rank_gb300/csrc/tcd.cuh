@@ -5,23 +5,27 @@
 //   phase 2  Y_b[t][c] = sum_{i in block b's range} H[i][t] W2[i][c]
 //   phase 3  y[t][c] = b2[c] + sum_b Y_b[t][c] (b ascending) (+ residual)
 //
-// Both contractions are D (fp32, tensor memory) += A (weights, shared
-// memory) x B (shared memory), B being the activations' high and low 16-bit
-// parts stacked as 2 bp columns (x = hi + lo, H = hi + lo: the two products
-// land in separate accumulator columns and are added in the epilogue).
+// Both contractions are D (fp32, tensor memory) += A x B with the
+// activations' high and low 16-bit parts stacked as A's rows (x = hi + lo,
+// H = hi + lo: row t < bp holds token t's high part, bp + t its low part,
+// so the two products land in separate accumulator lanes and are added in
+// the epilogue) and the weights as B, both in shared memory.
 // Shared-memory tiles use the 128-byte swizzle: rows of 64 16-bit elements
 // (128 bytes), 8-row atoms of 1024 bytes, 16-byte chunk c of row r stored at
 // chunk c ^ (r % 8) (the pattern follows the shared-memory address, so atoms
 // are 1024-byte aligned); TMA writes that form and the matrix descriptors
 // read it.
-//   phase 1: A = W1 rows, K-major (M = 128 neurons per half tile, K = 64
-//            columns per stage); B = x, K-major (N = 2 bp tokens).
-//   phase 2: A = W2 rows read as their transpose, M-major (M = 128 output
-//            columns as two 64-column halves, K = 64 neurons per stage);
-//            B = H^T, K-major.
+//   phase 1: A = x, K-major (M = 128 rows, 2 bp of them loaded; K = 64
+//            columns per stage); B = the block's W1 rows, K-major (N = its
+//            rows rounded up to 16, <= 256).
+//   phase 2: A = H^T, K-major (M = 128 rows, 2 bp loaded; K = 64 neurons
+//            per work item); B = the tile's columns of the W2 rows, read
+//            N-major (N = 256 output columns, or 128).
 // Roles: warp 0 issues the TMA copies, warp 1 the MMAs (and owns tensor
-// memory), warps 2-5 read the accumulators back.  Every wait is bounded; a
-// block that gives up records PI_ERR_TIMEOUT, lets its copies and MMAs
+// memory), warps 2-5 read the accumulators back.  The weight boxes of the
+// first stages are issued before the wait for the previous kernel (the
+// weights are not written by it); x and H^T after.  Every wait is bounded;
+// a block that gives up records PI_ERR_TIMEOUT, lets its copies and MMAs
 // finish (bounded) and frees its tensor memory before it exits.
 #pragma once
 
