@@ -182,12 +182,17 @@ pi_status pi_sparse_ffn(const pi_ffn_desc* desc, const pi_layer_weights* w,
                         pi_stream stream);
 
 /* Dense FFN over all n neurons, the comparison point of the sparse path.
- * The paper has no counterpart passage: this call is the baseline that the
- * sparse calls are measured against (every row read, no predictor):
+ * No passage of the method's pages defines it: this call is the baseline
+ * that the sparse calls are measured against (every row read, no
+ * predictor):
  *     y[t] = b2 + sum_i ReLU(W1_i . x[t] + b1_i) W2_i   (gated as above).
  * batch <= 32.  batch > 1 with d % 128 == 0 reads every row once for all
- * tokens on the tensor cores (the batched sparse path over all n neurons);
- * otherwise one persistent CUDA-core launch per token. */
+ * tokens on the tensor cores: tcgen05 MMAs with accumulators in tensor
+ * memory and operands staged by TMA where n % 64 == 0 and a block of the
+ * 1-per-SM grid holds at most 256 rows (PI_BATCH_LEGACY=1 in the environment
+ * keeps the mma.sync phases instead), the mma.sync phases of the batched
+ * sparse path over all n neurons otherwise; batch 1, or d % 128 != 0: one
+ * persistent CUDA-core launch per token. */
 pi_status pi_dense_ffn(const pi_ffn_desc* desc, const pi_layer_weights* w,
                        const float* x, int32_t batch, float* y, void* ws,
                        size_t ws_bytes, pi_stream stream);
