@@ -260,3 +260,36 @@ def test_dense_batched_tensor_memory_gated_batch32():
     for t in (0, 13, 31):
         want = oracle.dense_ffn(D.L, x[t])
         assert float(np.abs(y[t] - want).max()) <= Y_TOL * float(np.abs(want).max()), t
+
+
+def test_dense_batched_legacy_phases_subprocess():
+    """PI_BATCH_LEGACY=1 (read once per process, so in a child process)
+    keeps the dense batched FFN on the mma.sync phases: the same layer and
+    tokens against the oracle, at 16 and 32 padded tokens."""
+    import os
+    import subprocess
+    import sys
+    code = r'''
+import sys, numpy as np, torch
+import activation_sparse_decode_rank_gb300 as pi, oracle, synth
+sys.path.insert(0, "tests")
+from pihelp import DevLayer, Y_TOL, up
+dev = torch.device("cuda:0")
+D = DevLayer(synth.make_layer(1152, 4096, 64, "f16", alpha=0.9, density=0.1, seed=75), dev)
+for B in (8, 24):
+    x = synth.gen_x(78, B, B, 1152)
+    y = torch.full((B, 1152), float("nan"), device=dev)
+    pi.check(pi.pi_dense_ffn(D.desc, D.w, up(x, dev), B, y, D.workspace(B)))
+    torch.cuda.synchronize()
+    yh = y.cpu().numpy()
+    for t in (0, B - 1):
+        want = oracle.dense_ffn(D.L, x[t])
+        err = float(np.abs(yh[t] - want).max()) / float(np.abs(want).max())
+        assert err <= Y_TOL, (B, t, err)
+print("ok")
+'''
+    env = dict(os.environ, PI_BATCH_LEGACY="1")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
