@@ -162,3 +162,38 @@ def test_expected_union_matches_the_oracles_masks():
         _, o = plan(desc, B, p)
         assert o.union_rows == pytest.approx(unions.mean(), rel=0.03)
         assert o.active_rows == pytest.approx(masks.sum(axis=1).mean(), rel=0.03)
+
+
+# Measured on a GB300 (bench.py --sweep, OPT-13B-shaped layer d 5120,
+# n 20480, r 192, fp16, packed records, Zipf exponent 0.9, seed 5): the
+# sparse path's and the dense path's µs per step of B tokens at each
+# density.  Batch 1's sparse path is the fused layer kernel, larger
+# batches' the union path.
+SWEEP_US = {
+    # density: {B: (sparse, dense)}
+    0.02: {1: (19.4, 72.6), 4: (47.5, 75.9), 16: (75.8, 77.4), 32: (123.0, 83.7)},
+    0.05: {1: (22.9, 72.6), 4: (61.7, 76.1), 16: (104.9, 77.4), 32: (181.9, 83.6)},
+    0.10: {1: (27.1, 72.9), 4: (81.2, 76.1), 16: (148.2, 77.3), 32: (225.2, 83.4)},
+    0.25: {1: (40.8, 72.9), 4: (132.0, 76.4), 16: (192.9, 77.5), 32: (275.4, 83.7)},
+    0.50: {1: (66.9, 73.4), 4: (175.1, 76.6), 16: (219.2, 77.6), 32: (276.5, 84.0)},
+}
+
+
+@pytest.mark.parametrize("rho", sorted(SWEEP_US))
+def test_default_model_picks_the_measured_faster_path(rho):
+    # the built-in constants against the sweep they were fitted to: at every
+    # measured point the plan names the path that ran faster, and its
+    # estimate of that path lies within 10 % of the measurement
+    import synth
+
+    d, n, r, alpha = 5120, 20480, 192, 0.9
+    pz = synth.zipf_probs(n, alpha, synth.zipf_calibrate(n, alpha, rho))
+    desc = pi.make_desc(d, n, r, "f16", False, int((pz >= 0.5).sum()), packed=True)
+    for B, (sparse_us, dense_us) in SWEEP_US[rho].items():
+        st, o = plan(desc, B, pz.astype(np.float32), 0.0, 1)
+        assert st == pi.PI_OK
+        sp = pi.PI_PATH_FUSED if B == 1 else pi.PI_PATH_UNION
+        want = pi.PI_PATH_DENSE if dense_us < sparse_us else sp
+        assert o.path == want, (rho, B, [o.est_us[k] for k in range(pi.PI_PATHS)])
+        meas = min(sparse_us, dense_us)
+        assert o.est_us[want] == pytest.approx(meas, rel=0.10), (rho, B)
