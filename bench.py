@@ -750,7 +750,7 @@ def run_stack(args):
                      "traffic_how": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one "
                                      "launch (profiles/traffic.json)" if tr else
                                      "null: no capture of the current kernel source")},
-        "dense_ffn": {"us_per_token": dense_ms * 1e3 / L * L, "us_per_layer": dense_ms * 1e3 / L,
+        "dense_ffn": {"us_per_token": dense_ms * 1e3, "us_per_layer": dense_ms * 1e3 / L,
                       "tokens_per_s": 1e3 / dense_ms,
                       "achieved_gbs": dense_bytes / (dense_ms / 1e3) / 1e9,
                       "frac": dense_bytes / (dense_ms / 1e3) / 1e9 / peak},
